@@ -1,0 +1,222 @@
+/*
+ * wsw.h -- C ABI of libwsw.so, the decode-time weight-streaming hot path for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The calls cover the memory-bound mat-vec y = W.x that streams every weight byte
+ * once per decoded token, the block quantizer that turns the activation into int8
+ * blocks with absmax scales in front of the quantized mat-vec, the grouped MoE
+ * form of that mat-vec, the one-pass q8_0 KV-cache dequantizer and the
+ * small-batch prefill GEMM.  Each call is one or more hand-written CUDA kernels.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] "vulkan : dequant q8_0 KV once in coopmat1" (llama.cpp pull request)
+ *   [P2] "ggml-cuda: pad matmul weight rows to avoid cache-set aliasing"
+ *   [P3] "QuantizeQ8KK is thread-per-superblock: 95.5us/call against llama.cpp's
+ *        1.6us, and 41% of the ROCm decode gap"
+ *   [P4] "perf(vulkan): decode GEMV reads four elements per load, and the row lever
+ *        is dead"
+ *   [P5] "cuda: prefetch the next PTQ1_0 mat-vec's weights into L2 from the last CTAs"
+ *
+ * Conventions shared by every call
+ *   - Every pointer is a CUDA device pointer owned by the caller.  The library
+ *     allocates nothing and keeps no state between calls apart from per-device
+ *     kernel attributes set on first use.
+ *   - bf16 and binary16 (fp16) data travel as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous and stream-ordered; none synchronizes the host.
+ *   - Arguments are validated on the host before anything is launched.  A rejected
+ *     call returns a nonzero wsw_status and launches nothing.  A launch failure
+ *     returns WSW_ERR_CUDA (the CUDA error is not cleared; query it with
+ *     cudaGetLastError).  No kernel traps, asserts or spins without a bound.
+ *   - Row strides (ld, ldq, ldx) are in elements.  The elements between the row
+ *     length and the stride are padding and are never read ([P2] Overview: the
+ *     pad is zero-filled by the uploader, the kernels take the stride as given).
+ *   - A pointer or stride that is not aligned for 16-byte loads does not fail:
+ *     the weight load width degrades 16 -> 8 -> 4 -> 2 bytes until aligned, and
+ *     the result is bit-identical to the 16-byte path ([P4] "What shipped": the
+ *     load width degrades one step at a time when an offset is misaligned).
+ *     The exception is wsw_gemm_bf16, whose tensor-memory loads need 16-byte
+ *     alignment (WSW_ERR_MISALIGNED otherwise).
+ *   - Results do not depend on wsw_launch_opts: any rows_per_warp, load_bytes,
+ *     pdl or ctas_per_sm gives bit-identical output ([P4] "What did NOT work":
+ *     rows-per-workgroup variants verified bit-identical by full-output hash).
+ */
+#ifndef WSW_H
+#define WSW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WSW_ABI_VERSION 1
+
+typedef enum wsw_status {
+    WSW_OK = 0,
+    WSW_ERR_INVALID_ARG = 1, /* null pointer, bad size, stride or block size */
+    WSW_ERR_MISALIGNED = 2,  /* alignment that the call cannot degrade around */
+    WSW_ERR_UNSUPPORTED = 3, /* device is not sm_103 / shape beyond a stated limit */
+    WSW_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+    WSW_ERR_TIMEOUT = 6      /* reserved for bounded device-side waits */
+} wsw_status;
+
+/* Launch knobs.  Pass NULL for the defaults.  0 in a field means "choose". */
+typedef struct wsw_launch_opts {
+    int32_t rows_per_warp; /* output rows one warp reduces together: 1, 2 or 4
+                              (the pages' rows per workgroup, [P4] "What did NOT
+                              work"); 0 = 1 */
+    int32_t load_bytes;    /* cap on the weight load width: 16, 8, 4 or 2; 0 = 16 */
+    int32_t pdl;           /* 1 = launch with programmatic dependent launch: the
+                              kernel issues its first weight loads before waiting
+                              for the previous kernel in the stream ([P5]
+                              "Additional information": PDL on sm_90 and newer) */
+    int32_t ctas_per_sm;   /* resident CTAs per SM for persistent grids; 0 = auto */
+} wsw_launch_opts;
+
+/* Human-readable name of a wsw_status value (static storage, never NULL). */
+const char *wsw_status_string(int status);
+
+/* ABI version of the loaded library (WSW_ABI_VERSION it was built with). */
+int wsw_abi_version(void);
+
+/*
+ * wsw_quantize_q8 -- block quantizer for the activation ([P3] Cause: the amax
+ * scan over one superblock; [P3] Scope: quantize, then the quantized mat-vec).
+ *
+ * For each block of `block` consecutive values of a row:
+ *   amax = max |x|;  d = amax / 127 (fp32 division);
+ *   q = round_half_away_from_zero(x / d) (fp32 division by the fp32 d), in
+ *   [-127, 127];  an all-zero block gives d = +0 and q = 0.
+ * One thread per 8 elements and a warp-shuffle reduction of amax; each element is
+ * loaded once (the page's second defect, a second load per element, is avoided).
+ *
+ *   x       fp32 [rows][ldx]; the first n values of each row are quantized.
+ *   rows    >= 0;  n >= 0, a multiple of `block`;  ldx >= n.
+ *   block   32 (q8_0) or 256 (superblock).
+ *   q       int8 [rows][n], packed.
+ *   scales  block 32: binary16 [rows][n/32]; block 256: fp32 [rows][n/256].
+ * rows == 0 or n == 0 launches nothing and returns WSW_OK.
+ */
+int wsw_quantize_q8(const float *x, int64_t rows, int64_t n, int64_t ldx, int32_t block,
+                    int8_t *q, void *scales, void *stream, const wsw_launch_opts *opts);
+
+/*
+ * wsw_gemv_bf16 -- decode mat-vec with bf16 weights ([P4] opening paragraph: the
+ * decode GEMV streams ~52 GB of bf16 weights once per token and is bound by DRAM
+ * bandwidth; [P2] Overview: the row stride may exceed the row).
+ *
+ *   y[r] = alpha * sum_{k<K} W[r*ld + k] * x[k],  r < M,
+ * with bf16 x fp32 products accumulated in fp32.
+ *
+ *   W      bf16 [M][ld], row-major;  ld >= K.
+ *   x      fp32 [K] (not rounded to bf16).
+ *   y      fp32 [M]; must not overlap x.
+ * M == 0 launches nothing; K == 0 writes y = 0.
+ */
+int wsw_gemv_bf16(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const float *x,
+                  float alpha, float *y, void *stream, const wsw_launch_opts *opts);
+
+/*
+ * One link of a decode chain: y = alpha * W . x, as wsw_gemv_bf16.  x may point
+ * into an earlier link's y ([P5] Overview: consecutive mat-vecs of the decode
+ * graph, each paying a ramp-up and ramp-down in which DRAM idles).
+ */
+typedef struct wsw_gemv_link {
+    const uint16_t *W;
+    int64_t M, K, ld;
+    const float *x;
+    float alpha;
+    float *y;
+} wsw_gemv_link;
+
+/*
+ * wsw_gemv_bf16_chain -- launch n_links bf16 mat-vecs back to back on one stream,
+ * each one programmatically dependent on the one before ([P5] "Additional
+ * information": programmatic dependent launch is the sm_90+ tool for the idle
+ * window between chained mat-vecs).  Every link is validated before the first
+ * launch; the results equal n_links separate wsw_gemv_bf16 calls, bit for bit.
+ * opts->pdl = 0 turns the dependency off (plain stream order).
+ */
+int wsw_gemv_bf16_chain(int64_t n_links, const wsw_gemv_link *links, void *stream,
+                        const wsw_launch_opts *opts);
+
+/*
+ * wsw_gemv_q8_0 -- decode mat-vec with q8_0 weights and a q8_0 activation ([P3]
+ * Scope: the quantized mat-vec behind the quantizer).
+ *
+ *   y[r] = sum_b fp32(Wd[r][b]) * fp32(xd[b]) * (sum_{i<32} Wq[r*ldq + 32b+i] * xq[32b+i])
+ * with the block sums in exact int32 and the rest in fp32.
+ *
+ *   Wq   int8 [M][ldq];  K % 32 == 0, ldq % 32 == 0 and ldq >= K (a quantized
+ *        row stride must divide exactly into blocks, [P2] Overview).
+ *   Wd   binary16 [M][K/32], packed.
+ *   xq   int8 [K];  xd binary16 [K/32]  (as written by wsw_quantize_q8, block 32).
+ *   y    fp32 [M].
+ */
+int wsw_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, int64_t K, int64_t ldq,
+                  const int8_t *xq, const uint16_t *xd, float *y, void *stream,
+                  const wsw_launch_opts *opts);
+
+/*
+ * wsw_moe_gemv_q8_0 -- grouped MoE mat-vec over per-expert q8_0 weights ([P3]
+ * Cause and Scope: the MoE path quantizes m = T x top_k rows, then runs a grouped
+ * GEMM over the experts).
+ *
+ * For each row m < R with e = ids[m] in [0, E):
+ *   y[m][o] = gemv_q8_0(W_e, x_m)[o],  o < Mo,
+ * bit-identical to wsw_gemv_q8_0 on expert e's matrix and row m for R <= 256.
+ * Each expert that some row uses is streamed from memory once per call; experts
+ * no row uses are not read.  For R > 256 the rows of an expert are multiplied on
+ * the tensor cores with exact integer block sums; results then agree with the
+ * CUDA-core form within fp32 rounding, not bit for bit.
+ *
+ *   Wq   int8 [E][Mo][K];  Wd binary16 [E][Mo][K/32];  K % 32 == 0.
+ *   xq   int8 [R][K];  xd binary16 [R][K/32].
+ *   ids  int32 [R] (device).  A row whose id is outside [0, E) is skipped, its y
+ *        row is left untouched, and *err_flag (if err_flag != NULL) is set to a
+ *        nonzero value.  The library never clears *err_flag.
+ *   y    fp32 [R][Mo].
+ *   R <= 65536.
+ */
+int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E, int64_t Mo, int64_t K,
+                      const int8_t *xq, const uint16_t *xd, const int32_t *ids, int64_t R,
+                      float *y, int32_t *err_flag, void *stream, const wsw_launch_opts *opts);
+
+/*
+ * wsw_dequant_q8_0_kv -- dequantize one layer's q8_0 K (or V) cache once into a
+ * per-head-contiguous binary16 buffer ([P1] Overview and the stride discussion:
+ * the cache walks [dim][position][head] with a position stride of
+ * head_dim * heads elements; the scratch puts one head's positions back to back).
+ *
+ *   out[h][p][i] = f16_rn(fp32(d[p][h][i/32]) * q[p][h][i])
+ *
+ *   q     int8 [depth][heads][head_dim];  head_dim % 32 == 0.
+ *   d     binary16 [depth][heads][head_dim/32].
+ *   out   binary16 [heads][depth][head_dim]; must not overlap the inputs.
+ */
+int wsw_dequant_q8_0_kv(const int8_t *q, const uint16_t *d, int64_t depth, int64_t heads,
+                        int64_t head_dim, uint16_t *out, void *stream,
+                        const wsw_launch_opts *opts);
+
+/*
+ * wsw_gemm_bf16 -- small-batch prefill product on the tensor cores ([P2] Results:
+ * small-batch prefill streams the whole weight matrix for a short run of output
+ * rows; the weight's row stride may carry one extra 128-byte line).
+ *
+ *   Y[n][r] = sum_{k<K} W[r*ld + k] * X[n*ldx + k],  r < M, n < N,
+ * bf16 products accumulated in fp32.  Y row stride = M.
+ *
+ *   W   bf16 [M][ld];  X bf16 [N][ldx];  Y fp32 [N][M].
+ *   W and X 16-byte aligned; K, ld and ldx multiples of 8 (WSW_ERR_MISALIGNED
+ *   otherwise).
+ */
+int wsw_gemm_bf16(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const uint16_t *X,
+                  int64_t N, int64_t ldx, float *Y, void *stream, const wsw_launch_opts *opts);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WSW_H */
