@@ -1,0 +1,521 @@
+#!/usr/bin/env python
+"""Benchmark of the decode hot path on GB300: prints ONE JSON line.
+
+Workload (one GPU): the q8_0 decode mat-vec of a 14336 x 4096 weight (32-element
+int8 blocks with fp16 scales, quantized from N(0, 0.02) bf16) at batch 1, with the
+activation x (length 4096, N(0,1)) quantized to q8_0 in front of it, and the
+256-element superblock quantizer on x (length 4096) and on y (length 14336).
+
+  token  = quantize_q8(x_t, 32) -> gemv_q8_0(W_{t mod 16}, x_t) -> quantize_q8(y_t, 256)
+           and quantize_q8(x_t, 256); the four kernels are PDL-linked.
+  step   = a batch of 2048 tokens (distinct synthetic activations), captured once in
+           a CUDA graph and replayed.  16 distinct weight copies (1.0 GB) rotate, so
+           every GEMV streams weights that are not in the 129 MB L2.
+  value  = algorithmic bytes of the step / step time (GB/s), summed over ranks.
+
+The same line also reports: the GEMV kernel alone against the HBM roofline (CUDA
+events over back-to-back launches on distinct weight copies), the batch-1 quantizer
+in us/call (graph-amortised over 1000 calls), the 27B-shaped bf16 decode chain
+(64 layers x [QKV, O, gate/up, down] + lm_head, 257 PDL-linked mat-vecs, 43.16 GB
+per token), the end-to-end rate through the C ABI with host buffers, and the CPU
+oracle's rate on a bounded sample.
+
+--impl reference times the CPU oracle (the plain single-threaded C restatement) on
+the same workload, one token per step.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M, K = 14336, 4096
+NCOPY = 16
+TOKENS = 2048
+NOMINAL_HBM_GBS = 8000.0
+METRIC = "decode GEMV HBM GB/s and % of GB300 peak; Q8 quantizer us/call at batch 1"
+
+# algorithmic bytes per token (read + write, each byte once)
+B_Q32 = K * 4 + K + (K // 32) * 2                       # x in, q out, fp16 scales out
+B_GEMV = M * K + M * (K // 32) * 2 + K + (K // 32) * 2 + M * 4
+B_Q256_Y = M * 4 + M + (M // 256) * 4
+B_Q256_X = K * 4 + K + (K // 256) * 4
+B_TOKEN = B_Q32 + B_GEMV + B_Q256_Y + B_Q256_X
+
+CHAIN_LAYER = [(6144, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
+CHAIN_HEAD = (152064, 5120)
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """nvidia-smi samples (100 ms) taken while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [s for (t, s) in self.samples if self.t0 is not None and self.t0 - 0.05 <= t <= self.t1 + 0.05]
+        parsed = []
+        for r in rows:
+            f = [v.strip() for v in r.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                parsed.append((float(f[0]), float(f[1]), f[3:7]))
+            except ValueError:
+                continue
+        if not parsed:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for (_, _, fl) in parsed for i, v in enumerate(fl) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(p[0] for p in parsed), "sm_max_mhz": max(p[1] for p in parsed),
+                "reasons": reasons, "samples": len(parsed)}
+
+
+# -------------------------------------------------------------- our arm ----
+class Workload:
+    def __init__(self, wsw, torch, dev):
+        import weight_streaming_warp_gb300.synthetic as syn
+        self.wsw, self.torch = wsw, torch
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        self.Wq, self.Wd = [], []
+        for c in range(NCOPY):
+            Wf = torch.randn((M, K), generator=g, device=dev).mul_(0.02).to(torch.bfloat16).float()
+            q, d = wsw.quantize_q8(Wf, 32)  # weights quantized once, by the library
+            self.Wq.append(q)
+            self.Wd.append(d)
+            del Wf
+        self.X = syn.normal(0, "bench_x", (TOKENS, K), device=dev)
+        self.xq = torch.empty((TOKENS, K), dtype=torch.int8, device=dev)
+        self.xd = torch.empty((TOKENS, K // 32), dtype=torch.float16, device=dev)
+        self.Y = torch.empty((TOKENS, M), dtype=torch.float32, device=dev)
+        self.yq = torch.empty((TOKENS, M), dtype=torch.int8, device=dev)
+        self.ys = torch.empty((TOKENS, M // 256), dtype=torch.float32, device=dev)
+        self.xq2 = torch.empty((TOKENS, K), dtype=torch.int8, device=dev)
+        self.xs2 = torch.empty((TOKENS, K // 256), dtype=torch.float32, device=dev)
+        self._bind()
+
+    def _bind(self):
+        """Raw C-ABI entry points and pre-computed pointers (per-token launches)."""
+        L = self.wsw.load()
+        self.L = L
+        opts = self.wsw._COpts(0, 0, 1, 0)
+        self.opts = opts
+        self.popts = ctypes.byref(opts)
+        self.ptr = dict(X=self.X.data_ptr(), xq=self.xq.data_ptr(), xd=self.xd.data_ptr(), Y=self.Y.data_ptr(),
+                        yq=self.yq.data_ptr(), ys=self.ys.data_ptr(), xq2=self.xq2.data_ptr(),
+                        xs2=self.xs2.data_ptr())
+        self.wq = [w.data_ptr() for w in self.Wq]
+        self.wd = [w.data_ptr() for w in self.Wd]
+
+    def token(self, t, stream, rc):
+        L, p, o = self.L, self.ptr, self.popts
+        x = p["X"] + t * K * 4
+        xq, xd = p["xq"] + t * K, p["xd"] + t * (K // 32) * 2
+        y = p["Y"] + t * M * 4
+        rc |= L.wsw_quantize_q8(x, 1, K, K, 32, xq, xd, stream, o)
+        rc |= L.wsw_gemv_q8_0(self.wq[t % NCOPY], self.wd[t % NCOPY], M, K, K, xq, xd, y, stream, o)
+        rc |= L.wsw_quantize_q8(y, 1, M, M, 256, p["yq"] + t * M, p["ys"] + t * (M // 256) * 4, stream, o)
+        rc |= L.wsw_quantize_q8(x, 1, K, K, 256, p["xq2"] + t * K, p["xs2"] + t * (K // 256) * 4, stream, o)
+        return rc
+
+    def step(self, stream):
+        rc = 0
+        for t in range(TOKENS):
+            rc = self.token(t, stream, rc)
+        if rc:
+            raise RuntimeError("a launch failed: %s" % self.wsw.status_string(rc))
+
+
+def _graph(torch, fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn(ctypes.c_void_p(s.cuda_stream))  # first use (per-device set-up) outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return g
+
+
+def _time_graph(torch, g, reps):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1000.0 / reps
+
+
+def _traffic_record(kernel_file):
+    """DRAM traffic per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        src = open(os.path.join(ROOT, "weight_streaming_warp_gb300", "csrc", kernel_file), "rb").read()
+        r = rec.get(kernel_file)
+        if r and r.get("source_sha256") == hashlib.sha256(src).hexdigest():
+            return r["bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+def measure_gemv_kernel(torch, wl):
+    """gemv_q8_0 alone: 256 back-to-back PDL launches over the 16 weight copies."""
+    n = 256
+
+    def fn(stream):
+        rc = 0
+        for i in range(n):
+            rc |= wl.L.wsw_gemv_q8_0(wl.wq[i % NCOPY], wl.wd[i % NCOPY], M, K, K, wl.ptr["xq"], wl.ptr["xd"],
+                                     wl.ptr["Y"] + (i % 64) * M * 4, stream, wl.popts)
+        assert rc == 0
+
+    g = _graph(torch, fn)
+    _time_graph(torch, g, 3)
+    times = [_time_graph(torch, g, 1) / n for _ in range(10)]
+    return statistics.median(times), min(times), max(times)
+
+
+def measure_quantizer(torch, wl):
+    """Batch-1 quantizer calls back to back in a graph: us per call."""
+    n = 1000
+    out = {}
+    for (name, length, block, src) in (("q8_0_n4096", K, 32, "X"), ("superblock_n4096", K, 256, "X"),
+                                       ("superblock_n14336", M, 256, "Y")):
+        qs = wl.xq if length == K else wl.yq
+        sc = wl.xd if block == 32 else (wl.xs2 if length == K else wl.ys)
+
+        def fn(stream, length=length, block=block, src=src, qs=qs, sc=sc):
+            rc = 0
+            for i in range(n):
+                t = i % TOKENS
+                rc |= wl.L.wsw_quantize_q8(wl.ptr[src] + t * length * 4, 1, length, length, block,
+                                           qs.data_ptr() + t * length,
+                                           sc.data_ptr() + t * (length // block) * sc.element_size(),
+                                           stream, wl.popts)
+            assert rc == 0
+
+        g = _graph(torch, fn)
+        _time_graph(torch, g, 2)
+        out[name] = round(statistics.median(_time_graph(torch, g, 1) for _ in range(5)) / n * 1e6, 3)
+    return out
+
+
+def measure_chain(torch, wsw, dev):
+    """27B-shaped dense decode chain, bf16 weights N(0, 0.02), one token per replay."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    shapes = [s for _ in range(64) for s in CHAIN_LAYER] + [CHAIN_HEAD]
+    Ws, ys = [], []
+    for (Mi, Ki) in shapes:
+        Ws.append(torch.randn((Mi, Ki), generator=g, device=dev, dtype=torch.float32).mul_(0.02).to(torch.bfloat16))
+        ys.append(torch.empty(Mi, dtype=torch.float32, device=dev))
+    x0 = torch.randn(CHAIN_LAYER[0][1], generator=g, device=dev)
+    links = []
+    for i, (Mi, Ki) in enumerate(shapes):
+        x = x0 if i == 0 else ys[i - 1][:Ki]
+        links.append((Ws[i], Ki, x, 1.0 / (0.02 * math.sqrt(Ki)), ys[i]))
+    nbytes = sum(Mi * Ki * 2 + Ki * 4 + Mi * 4 for (Mi, Ki) in shapes)
+    res = {}
+    graphs = {}
+    for pdl in (1, 0):
+        graphs[pdl] = _graph(torch, lambda stream, pdl=pdl: wsw.gemv_bf16_chain(links, opts={"pdl": pdl}))
+        _time_graph(torch, graphs[pdl], 2)
+    t = {1: [], 0: []}
+    for rep in range(6):  # paired, alternating order
+        for pdl in ((1, 0) if rep % 2 == 0 else (0, 1)):
+            t[pdl].append(_time_graph(torch, graphs[pdl], 1))
+    for pdl in (1, 0):
+        med = statistics.median(t[pdl])
+        res["pdl" if pdl else "no_pdl"] = {"ms_per_token": round(med * 1e3, 4),
+                                          "GBps": round(nbytes / med / 1e9, 1),
+                                          "tok_per_s": round(1.0 / med, 2),
+                                          "min_ms": round(min(t[pdl]) * 1e3, 4), "max_ms": round(max(t[pdl]) * 1e3, 4)}
+    ok = all(bool(torch.isfinite(y).all()) for y in ys[-2:])
+    del graphs, Ws, ys, links
+    torch.cuda.empty_cache()
+    res["bytes_per_token"] = nbytes
+    res["launches_per_token"] = len(shapes)
+    res["finite"] = ok
+    return res
+
+
+def measure_e2e(torch, wl, dev, steps):
+    """Through the C ABI with host buffers: per step, copy the batch's activations
+    from pinned host memory, launch every token, copy y back."""
+    xh = wl.X.cpu().pin_memory()
+    yh = torch.empty((TOKENS, M), dtype=torch.float32).pin_memory()
+    s = torch.cuda.current_stream()
+    stream = ctypes.c_void_p(s.cuda_stream)
+    n = max(1, min(steps, 3))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        wl.X.copy_(xh, non_blocking=True)
+        wl.step(stream)
+        yh.copy_(wl.Y, non_blocking=True)
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(B_TOKEN * TOKENS / dt / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": TOKENS * K * 4, "d2h_bytes_per_step": TOKENS * M * 4,
+            "ms_per_step": round(dt * 1e3, 3), "steps": n}
+
+
+_CPU_INPUTS = None
+
+
+def _cpu_inputs():
+    """Host inputs of the CPU oracle: one q8_0 weight copy and 8 activations."""
+    global _CPU_INPUTS
+    if _CPU_INPUTS is None:
+        import torch
+        import oracle as orc
+        import weight_streaming_warp_gb300.synthetic as syn
+        W = syn.normal(0, "cpu_W", (M, K), 0.02, torch.bfloat16).float().numpy()
+        Wq, Wd = orc.quantize_q8(W, 32)
+        X = syn.normal(0, "cpu_x", (8, K)).numpy()
+        _CPU_INPUTS = (Wq, Wd, X)
+    return _CPU_INPUTS
+
+
+def cpu_oracle_tokens(n):
+    """Run n tokens of the workload through the oracle (quantize x, q8_0 GEMV over
+    all 14336 rows, the two superblock quantizations); returns elapsed seconds."""
+    import numpy as np
+    import oracle as orc
+    Wq, Wd, X = _cpu_inputs()
+    t0 = time.perf_counter()
+    for i in range(n):
+        x = X[i % 8:i % 8 + 1]
+        xq, xd = orc.quantize_q8(x, 32)
+        y = orc.gemv_q8_0(Wq, Wd, xq[0], xd[0]).astype(np.float32)
+        orc.quantize_q8(y[None, :], 256)
+        orc.quantize_q8(x, 256)
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_rate(seconds=10.0):
+    """GB/s of the oracle over about `seconds` of host time (at least 2 tokens)."""
+    _cpu_inputs()
+    per = cpu_oracle_tokens(1)
+    n = max(2, int(seconds / max(per, 1e-6)))
+    el = cpu_oracle_tokens(n)
+    return B_TOKEN * n / el / 1e9, n, el
+
+
+def run_ours(args):
+    import torch
+    import weight_streaming_warp_gb300 as wsw
+    from weight_streaming_warp_gb300 import build as wbuild
+
+    rank, world, local = _dist()
+    wbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    wl = Workload(wsw, torch, dev)
+    step_graph = _graph(torch, wl.step)
+
+    for _ in range(args.warmup):
+        step_graph.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record()
+    for _ in range(args.steps):
+        step_graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if pg:
+        pg.barrier()
+    clocks.mark(t0, t1)
+    clk = clocks.stop()
+    elapsed = e0.elapsed_time(e1) / 1000.0
+    if pg:
+        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        elapsed = float(tt.item())
+    step_s = elapsed / args.steps
+    value = B_TOKEN * TOKENS * world / step_s / 1e9
+
+    peak, peak_kind = _peaks()
+    k_med, k_min, k_max = measure_gemv_kernel(torch, wl)
+    achieved = B_GEMV / k_med / 1e9
+    quant = measure_quantizer(torch, wl)
+    e2e = measure_e2e(torch, wl, dev, args.steps)
+    del step_graph
+    chain = measure_chain(torch, wsw, dev) if rank == 0 else None
+
+    if pg:
+        pg.barrier()
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+    cpu_v, cpu_n, cpu_s = cpu_oracle_rate(seconds=10.0) if world == 1 else (None, 0, 0.0)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8 x int8 -> int32 blocks, fp32 scale/accumulate (q8_0); fp32 quantizer",
+        "data": "synthetic: seeded N(0,0.02) bf16 weights quantized to q8_0, N(0,1) activations",
+        "config": {"workload": "q8_0 decode GEMV 14336x4096 batch 1 + q8_0 quantizer (n=4096) + "
+                               "superblock quantizer (n=4096, n=14336), PDL-linked",
+                   "tokens_per_step": TOKENS, "bytes_per_token": B_TOKEN,
+                   "weight_copies": NCOPY, "weight_bytes_per_copy": B_GEMV - K - (K // 32) * 2 - M * 4,
+                   "l2": "inputs larger than L2: 16 rotating weight copies (1.0 GB) vs 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "timing": "CUDA events around K replays of a CUDA graph of one step"},
+        "pct_of_measured_hbm_peak": round(100.0 * value / world / peak, 2),
+        "pct_of_nominal_8TBps": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
+        "quantizer_us_per_call": quant,
+        "roofline": {"kernel": "gemv_q8_0_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy)",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": _traffic_record("gemv_q8_0.cu"),
+                     "algorithmic_bytes_per_launch": B_GEMV,
+                     "launch_us": {"median": round(k_med * 1e6, 3), "min": round(k_min * 1e6, 3),
+                                   "max": round(k_max * 1e6, 3)}},
+        "chain_27b_bf16": chain,
+        "e2e": e2e,
+        "gpu_launches": 4 * TOKENS * args.steps,
+        "clocks": clk,
+        "cpu_baseline": None if cpu_v is None else {
+            "value": round(cpu_v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d full tokens (quantize + 14336x4096 q8_0 GEMV + 2 superblock quantizations) in %.1f s"
+                      % (cpu_n, cpu_s)},
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    oracle.lib()
+    _cpu_inputs()
+    cpu_oracle_tokens(args.warmup)
+    el = cpu_oracle_tokens(args.steps)
+    value = B_TOKEN * args.steps / el / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp64 oracle",
+        "data": "synthetic", "config": {"workload": "q8_0 decode GEMV 14336x4096 batch 1 + quantizers (one token per step)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "one full token per step (all 14336 rows)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

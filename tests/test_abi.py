@@ -1,0 +1,109 @@
+"""The C-ABI library loads on a machine without a GPU, exports every function that
+include/wsw.h declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_streaming_warp_gb300 as wsw
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(wsw_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from weight_streaming_warp_gb300 import build
+    build.build()
+    return wsw.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"wsw_quantize_q8", "wsw_gemv_bf16", "wsw_gemv_q8_0", "wsw_moe_gemv_q8_0",
+            "wsw_dequant_q8_0_kv", "wsw_gemm_bf16", "wsw_gemv_bf16_chain"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+
+
+def test_abi_version_and_status_strings(lib):
+    assert wsw.abi_version() == 1
+    assert wsw.status_string(0) == "WSW_OK"
+    assert wsw.status_string(1) == "WSW_ERR_INVALID_ARG"
+    assert wsw.status_string(2) == "WSW_ERR_MISALIGNED"
+    assert wsw.status_string(99) == "WSW_ERR_UNKNOWN"
+
+
+INVALID, MISALIGNED, UNSUPPORTED = 1, 2, 3
+P = ctypes.c_void_p
+
+
+class _Opts(ctypes.Structure):
+    _fields_ = [("rows_per_warp", ctypes.c_int32), ("load_bytes", ctypes.c_int32),
+                ("pdl", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32)]
+
+
+def test_quantize_rejects_on_host(lib):
+    f = lib.wsw_quantize_q8
+    x = P(4096)
+    assert f(x, 1, 64, 64, 16, P(4096), P(4096), None, None) == INVALID  # block size
+    assert f(x, 1, 48, 64, 32, P(4096), P(4096), None, None) == INVALID  # n % block
+    assert f(x, 1, 64, 32, 32, P(4096), P(4096), None, None) == INVALID  # ldx < n
+    assert f(None, 1, 64, 64, 32, P(4096), P(4096), None, None) == INVALID
+    assert f(x, -1, 64, 64, 32, P(4096), P(4096), None, None) == INVALID
+    assert f(P(4098), 1, 64, 64, 32, P(4096), P(4096), None, None) == MISALIGNED
+    assert f(x, 0, 64, 64, 32, None, None, None, None) == 0  # empty: nothing to do
+    assert f(x, 3, 0, 0, 256, None, None, None, None) == 0
+    bad = _Opts(3, 0, 0, 0)
+    assert f(x, 1, 64, 64, 32, P(4096), P(4096), None, ctypes.byref(bad)) == INVALID
+    bad = _Opts(0, 12, 0, 0)
+    assert f(x, 1, 64, 64, 32, P(4096), P(4096), None, ctypes.byref(bad)) == INVALID
+
+
+def test_gemv_rejects_on_host(lib):
+    f = lib.wsw_gemv_bf16
+    assert f(P(4096), 4, 64, 32, P(4096), ctypes.c_float(1.0), P(4096), None, None) == INVALID
+    assert f(None, 4, 64, 64, P(4096), ctypes.c_float(1.0), P(4096), None, None) == INVALID
+    assert f(P(4097), 4, 64, 64, P(4096), ctypes.c_float(1.0), P(4096), None, None) == MISALIGNED
+    assert f(P(4096), 0, 64, 64, None, ctypes.c_float(1.0), None, None, None) == 0
+    g = lib.wsw_gemv_q8_0
+    assert g(P(4096), P(4096), 4, 48, 64, P(4096), P(4096), P(4096), None, None) == INVALID  # K % 32
+    assert g(P(4096), P(4096), 4, 64, 80, P(4096), P(4096), P(4096), None, None) == INVALID  # ldq % 32
+    assert g(P(4096), P(4096), 4, 64, 32, P(4096), P(4096), P(4096), None, None) == INVALID  # ldq < K
+    assert g(P(4096), P(4097), 4, 64, 64, P(4096), P(4096), P(4096), None, None) == MISALIGNED
+
+
+def test_other_calls_reject_on_host(lib):
+    m = lib.wsw_moe_gemv_q8_0
+    assert m(P(4096), P(4096), 8, 16, 48, P(4096), P(4096), P(4096), 4, P(4096), None, None, None) == INVALID
+    assert m(P(4096), P(4096), 4096, 16, 64, P(4096), P(4096), P(4096), 4, P(4096), None, None, None) == UNSUPPORTED
+    assert m(P(4096), P(4096), 8, 16, 64, P(4096), P(4096), P(4096), 70000, P(4096), None, None, None) == UNSUPPORTED
+    assert m(P(4096), P(4096), 8, 16, 64, P(4096), P(4096), P(4096), 0, P(4096), None, None, None) == 0
+    d = lib.wsw_dequant_q8_0_kv
+    assert d(P(4096), P(4096), 16, 4, 100, P(4096), None, None) == INVALID
+    assert d(P(4096), P(4097), 16, 4, 128, P(4096), None, None) == MISALIGNED
+    assert d(P(4096), P(4096), 0, 4, 128, P(4096), None, None) == 0
+    g = lib.wsw_gemm_bf16
+    assert g(P(4096), 16, 64, 64, P(4104), 8, 64, P(4096), None, None) == MISALIGNED
+    assert g(P(4096), 16, 60, 64, P(4096), 8, 64, P(4096), None, None) == MISALIGNED
+    assert g(P(4096), 16, 64, 32, P(4096), 8, 64, P(4096), None, None) == INVALID
+    c = lib.wsw_gemv_bf16_chain
+    assert c(-1, None, None, None) == INVALID
+    assert c(0, None, None, None) == 0
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    monkeypatch.setattr(wsw, "_lib", None)
+    monkeypatch.setattr(wsw, "_LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(wsw.WswError):
+        wsw.load()

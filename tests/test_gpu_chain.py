@@ -1,0 +1,97 @@
+"""The PDL-linked decode chain: y_i feeds x_{i+1}.  Checked end to end against the
+fp64 oracle chain, and bit for bit against the same links launched one at a time
+without programmatic dependent launch, eagerly and inside a CUDA graph."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL_BF16, bf16_bits, need_gpu
+from weight_streaming_warp_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+# one decoder layer of the 27B-shaped dense model: (name, M, K)
+LAYER = [("qkv", 6144, 5120), ("o", 5120, 5120), ("gate_up", 34816, 5120), ("down", 5120, 17408)]
+LM_HEAD = ("lm_head", 152064, 5120)
+
+
+def _links(n_layers, dims_scale=1, lm_head=True):
+    shapes = []
+    for layer in range(n_layers):
+        for (nm, M, K) in LAYER:
+            shapes.append(("%s%d" % (nm, layer), M // dims_scale, K // dims_scale))
+    if lm_head:
+        shapes.append((LM_HEAD[0], LM_HEAD[1] // dims_scale, LM_HEAD[2] // dims_scale))
+    return shapes
+
+
+def _build(shapes, seed=0):
+    Ws = [syn.normal(seed, nm, (M, K), 0.02, torch.bfloat16, device="cuda") for (nm, M, K) in shapes]
+    ys = [torch.empty(M, dtype=torch.float32, device="cuda") for (_, M, _) in shapes]
+    x0 = syn.normal(seed, "x0", (shapes[0][2],)).cuda()
+    links = []
+    for i, (nm, M, K) in enumerate(shapes):
+        x = x0 if i == 0 else ys[i - 1][:K]  # the previous output, truncated to this K
+        links.append((Ws[i], K, x, 1.0 / (0.02 * math.sqrt(K)), ys[i]))
+    return Ws, ys, x0, links
+
+
+def _oracle_chain(orc, Ws, x0, shapes):
+    x = x0.double().cpu().numpy()
+    outs = []
+    for W, (nm, M, K) in zip(Ws, shapes):
+        y = orc.gemv_bf16(bf16_bits(W), x[:K], 1.0 / (0.02 * math.sqrt(K)))
+        outs.append(y)
+        x = y
+    return outs
+
+
+def _assert_chain_close(ys, ref, what):
+    for i, (y, r) in enumerate(zip(ys, ref)):
+        y = y.cpu().double().numpy()
+        rel = np.linalg.norm(y - r) / np.linalg.norm(r)
+        assert np.isfinite(y).all() and rel <= TOL_BF16, "%s link %d: %.3g" % (what, i, rel)
+
+
+def test_two_layers_and_lm_head_full_shapes(orc):
+    wsw = need_gpu()
+    shapes = _links(2)
+    Ws, ys, x0, links = _build(shapes)
+    wsw.gemv_bf16_chain(links)
+    torch.cuda.synchronize()
+    ref = _oracle_chain(orc, Ws, x0, shapes)
+    _assert_chain_close(ys, ref, "pdl chain")
+    pdl = [y.clone() for y in ys]
+    # plain stream order, one call per link
+    for (W, K, x, a, y) in links:
+        wsw.gemv_bf16(W, x, alpha=a, K=K, out=y)
+    for a, b in zip(pdl, ys):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_many_links_in_a_cuda_graph(orc):
+    """64 small layers + head (257 links), PDL edges captured in a CUDA graph."""
+    wsw = need_gpu()
+    shapes = _links(64, dims_scale=16)
+    Ws, ys, x0, links = _build(shapes, seed=1)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        wsw.gemv_bf16_chain(links)  # warm-up (and per-device set-up) before capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        wsw.gemv_bf16_chain(links)
+    for y in ys:
+        y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    ref = _oracle_chain(orc, Ws, x0, shapes)
+    _assert_chain_close(ys, ref, "graph chain")
+    graph_out = [y.clone() for y in ys]
+    wsw.gemv_bf16_chain(links, opts={"pdl": 0})
+    for a, b in zip(graph_out, ys):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))

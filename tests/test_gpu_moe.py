@@ -1,0 +1,119 @@
+"""moe_gemv_q8_0 on the GPU: against the fp64 oracle (tolerance 1e-4), bit for bit
+against the dense gemv_q8_0 on each row's expert, bad ids, unused experts."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL_Q8, check_tol, mag_q8, need_gpu, u16_to_torch
+from weight_streaming_warp_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+E, TOPK = 128, 8
+PROJ = {"gate_up": (1536, 2048), "down": (2048, 768)}
+
+
+def _expert_weights(orc, name, Mo, K, experts):
+    """q8_0 weights quantized from N(0, 0.02) bf16 for the listed experts; the
+    others hold NaN scales (they must never be read)."""
+    Wq = np.zeros((E, Mo, K), np.int8)
+    Wd = np.full((E, Mo, K // 32), 0x7E00, np.uint16)  # binary16 NaN
+    for e in experts:
+        W = syn.normal(0, "%s_e%d" % (name, e), (Mo, K), 0.02, torch.bfloat16).float().numpy()
+        Wq[e], Wd[e] = orc.quantize_q8(W, 32)
+    return Wq, Wd
+
+
+@pytest.fixture(scope="module")
+def moe_weights(orc):
+    return {p: _expert_weights(orc, p, Mo, K, range(E)) for p, (Mo, K) in PROJ.items()}
+
+
+def _acts(orc, T, K, name):
+    x = syn.normal(0, "%s_x%d" % (name, T), (T * TOPK, K)).numpy()
+    return orc.quantize_q8(x, 32)
+
+
+def _run(wsw, Wq, Wd, xq, xd, ids, opts=None):
+    return wsw.moe_gemv_q8_0(torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda(),
+                             torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda(),
+                             torch.from_numpy(ids).cuda(), opts=opts)
+
+
+@pytest.mark.parametrize("proj", ["gate_up", "down"])
+@pytest.mark.parametrize("T", [1, 16, 512])
+def test_config_moe(orc, moe_weights, proj, T):
+    wsw = need_gpu()
+    Mo, K = PROJ[proj]
+    Wq, Wd = moe_weights[proj]
+    ids = syn.routing(0, "route%d" % T, T, E, TOPK).numpy()
+    xq, xd = _acts(orc, T, K, proj)
+    y = _run(wsw, Wq, Wd, xq, xd, ids).cpu().numpy()
+    R = T * TOPK
+    rows = np.arange(R) if R <= 128 else np.unique(np.random.default_rng(T).integers(0, R, 64))
+    for m in rows:
+        e = ids[m]
+        y64 = orc.gemv_q8_0(Wq[e], Wd[e], xq[m], xd[m])
+        check_tol(y[m], y64, mag_q8(Wq[e], Wd[e], xq[m], xd[m]), TOL_Q8, "%s T=%d row %d" % (proj, T, m))
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_rows_equal_dense_gemv_bitwise(orc, moe_weights, T):
+    wsw = need_gpu()
+    Mo, K = PROJ["gate_up"]
+    Wq, Wd = moe_weights["gate_up"]
+    ids = syn.routing(0, "route%d" % T, T, E, TOPK).numpy()
+    xq, xd = _acts(orc, T, K, "gate_up")
+    y = _run(wsw, Wq, Wd, xq, xd, ids)
+    for m in range(T * TOPK):
+        e = ids[m]
+        yd = wsw.gemv_q8_0(torch.from_numpy(Wq[e]).cuda(), u16_to_torch(Wd[e], torch.float16).cuda(),
+                           torch.from_numpy(xq[m]).cuda(), u16_to_torch(xd[m], torch.float16).cuda())
+        assert torch.equal(yd.view(torch.int32), y[m].view(torch.int32)), m
+
+
+def test_unused_experts_are_not_read(orc):
+    wsw = need_gpu()
+    Mo, K = 256, 512
+    T = 4
+    ids = syn.routing(5, "few", T, E, TOPK).numpy()
+    Wq, Wd = _expert_weights(orc, "few", Mo, K, sorted(set(ids.tolist())))
+    xq, xd = _acts(orc, T, K, "few")
+    y = _run(wsw, Wq, Wd, xq, xd, ids).cpu().numpy()
+    assert np.isfinite(y).all()
+    for m in range(T * TOPK):
+        e = ids[m]
+        check_tol(y[m], orc.gemv_q8_0(Wq[e], Wd[e], xq[m], xd[m]), mag_q8(Wq[e], Wd[e], xq[m], xd[m]), TOL_Q8)
+
+
+def test_bad_ids_set_the_flag_and_skip_rows(orc):
+    wsw = need_gpu()
+    Mo, K, En = 64, 128, 4
+    g = np.random.default_rng(9)
+    Wq = g.integers(-127, 128, size=(En, Mo, K)).astype(np.int8)
+    Wd = g.integers(0x1000, 0x2000, size=(En, Mo, K // 32)).astype(np.uint16)
+    xq = g.integers(-127, 128, size=(6, K)).astype(np.int8)
+    xd = g.integers(0x1000, 0x2000, size=(6, K // 32)).astype(np.uint16)
+    ids = np.array([0, 4, 3, -1, 1, 3], np.int32)
+    y = torch.full((6, Mo), 5.0, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wsw.moe_gemv_q8_0(torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda(),
+                      torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda(),
+                      torch.from_numpy(ids).cuda(), out=y, err_flag=err)
+    assert err.item() != 0
+    yc = y.cpu().numpy()
+    assert (yc[1] == 5.0).all() and (yc[3] == 5.0).all()
+    y64, bad = orc.moe_gemv_q8_0(Wq, Wd, xq, xd, ids)
+    assert bad == 2
+    for m in (0, 2, 4, 5):
+        check_tol(yc[m], y64[m], mag_q8(Wq[ids[m]], Wd[ids[m]], xq[m], xd[m]), TOL_Q8)
+
+
+def test_empty_and_single_row():
+    wsw = need_gpu()
+    Wq = torch.zeros((2, 8, 32), dtype=torch.int8, device="cuda")
+    Wd = torch.zeros((2, 8, 1), dtype=torch.float16, device="cuda")
+    y = wsw.moe_gemv_q8_0(Wq, Wd, torch.zeros((0, 32), dtype=torch.int8, device="cuda"),
+                          torch.zeros((0, 1), dtype=torch.float16, device="cuda"),
+                          torch.zeros(0, dtype=torch.int32, device="cuda"))
+    assert y.numel() == 0

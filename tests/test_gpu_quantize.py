@@ -1,0 +1,103 @@
+"""quantize_q8 on the GPU against the oracle: bit-exact q bytes and scale bits."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import f16_bits, need_gpu
+from weight_streaming_warp_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(wsw, orc, x_host: torch.Tensor, block, xdev=None, opts=None):
+    xdev = x_host.cuda() if xdev is None else xdev
+    q, s = wsw.quantize_q8(xdev, block, opts=opts)
+    torch.cuda.synchronize()
+    xq = x_host.numpy() if x_host.dim() == 2 else x_host.numpy()[None, :]
+    qr, sr = orc.quantize_q8(np.ascontiguousarray(xq), block)
+    qg = q.cpu().numpy().reshape(qr.shape)
+    assert (qg == qr).all(), "q differs at %s" % (np.argwhere(qg != qr)[:5],)
+    if block == 32:
+        sg = f16_bits(s).reshape(sr.shape)
+    else:
+        sg = s.cpu().numpy().reshape(sr.shape)
+    assert (sg.view(np.uint32 if block == 256 else np.uint16) ==
+            sr.view(np.uint32 if block == 256 else np.uint16)).all()
+    return q, s
+
+
+@pytest.mark.parametrize("block", [32, 256])
+@pytest.mark.parametrize("rows,n", [(1, 4096), (1, 14336), (3, 512), (7, 768), (1, 256), (5, 2048)])
+def test_quantize_matches_oracle(orc, block, rows, n):
+    wsw = need_gpu()
+    x = syn.normal(0, "q%d_%d" % (rows, n), (rows, n))
+    _compare(wsw, orc, x, block)
+
+
+@pytest.mark.parametrize("block", [32, 256])
+def test_quantize_varied_block_scales(orc, block):
+    """Blocks whose magnitudes span 1e-6 .. 1e4, zero blocks and single spikes."""
+    wsw = need_gpu()
+    nb = 64
+    x = syn.normal(1, "v", (nb, block)).double()
+    scale = 10.0 ** torch.linspace(-6, 4, nb, dtype=torch.float64)
+    x = (x * scale[:, None]).float()
+    x[3] = 0.0
+    x[5] = 0.0
+    x[5, 7] = -2.5
+    x = x.reshape(1, nb * block)
+    _compare(wsw, orc, x, block)
+
+
+def test_quantize_ties_and_exact_grid(orc):
+    wsw = need_gpu()
+    x = torch.zeros(1, 64)
+    x[0, 0] = 127.0
+    x[0, 1:9] = torch.tensor([2.5, -2.5, 0.5, -0.5, 1.5, 126.5, -3.5, 0.49999997])
+    k = torch.arange(-127, -95, dtype=torch.float32)
+    x[0, 32:64] = k * 2.0 ** -7
+    q, s = _compare(wsw, orc, x, 32)
+    assert q[0, 1:9].tolist() == [3, -3, 1, -1, 2, 127, -4, 0]
+    assert q[0, 32:64].tolist() == k.int().tolist()
+
+
+@pytest.mark.parametrize("block", [32, 256])
+def test_quantize_moe_batch_shape(orc, block):
+    """T = 512 tokens x top_k 8 rows of the 2048-wide hidden state."""
+    wsw = need_gpu()
+    x = syn.normal(2, "moe", (4096, 2048))
+    _compare(wsw, orc, x, block)
+
+
+def test_quantize_strided_and_misaligned_rows(orc):
+    wsw = need_gpu()
+    for pad in (4, 1, 3):  # ldx = n + pad: vector path for 4, element path otherwise
+        n = 256
+        big = syn.normal(3, "s%d" % pad, (6, n + pad))
+        xdev = big.cuda()[:, :n]
+        _compare(wsw, orc, big[:, :n].contiguous(), 32, xdev=xdev)
+    # base address not 16-byte aligned
+    flat = syn.normal(3, "m", (1, 1 + 512))
+    xdev = flat.cuda()[0, 1:]
+    _compare(wsw, orc, flat[0, 1:].contiguous(), 256, xdev=xdev)
+
+
+def test_quantize_launch_options_do_not_change_bits(orc):
+    wsw = need_gpu()
+    x = syn.normal(4, "o", (2, 4096)).cuda()
+    ref = [t.clone() for t in wsw.quantize_q8(x, 32)]
+    for opts in ({"pdl": 1}, {"ctas_per_sm": 1}, {"rows_per_warp": 4, "load_bytes": 2}):
+        got = wsw.quantize_q8(x, 32, opts=opts)
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[1].view(torch.int16), ref[1].view(torch.int16))
+
+
+def test_quantize_empty_inputs():
+    wsw = need_gpu()
+    x = torch.empty((0, 64), device="cuda")
+    q, s = wsw.quantize_q8(x, 32)
+    assert q.numel() == 0 and s.numel() == 0
+    x = torch.empty((3, 0), device="cuda")
+    q, s = wsw.quantize_q8(x, 256)
+    assert q.numel() == 0
+    with pytest.raises(wsw.WswError):
+        wsw.quantize_q8(torch.zeros(48, device="cuda"), 32)
