@@ -31,9 +31,9 @@
  *   - Row strides (ld, ldq, ldx) are in elements.  The elements between the row
  *     length and the stride are padding and are never read ([P2] Overview: the
  *     pad is zero-filled by the uploader, the kernels take the stride as given).
- *   - A pointer or stride that is not aligned for 16-byte loads does not fail:
- *     the weight load width degrades 16 -> 8 -> 4 -> 2 bytes until aligned, and
- *     the result is bit-identical to the 16-byte path ([P4] "What shipped": the
+ *   - A pointer or stride that is not aligned for 32-byte loads does not fail:
+ *     the weight load width degrades 32 -> 16 -> 8 -> 4 -> 2 bytes until aligned,
+ *     and the result is bit-identical to the 32-byte path ([P4] "What shipped": the
  *     load width degrades one step at a time when an offset is misaligned).
  *     The exception is wsw_gemm_bf16, whose tensor-memory loads need 16-byte
  *     alignment (WSW_ERR_MISALIGNED otherwise).
@@ -66,8 +66,9 @@ typedef enum wsw_status {
 typedef struct wsw_launch_opts {
     int32_t rows_per_warp; /* output rows one warp reduces together: 1, 2 or 4
                               (the pages' rows per workgroup, [P4] "What did NOT
-                              work"); 0 = 1 */
-    int32_t load_bytes;    /* cap on the weight load width: 16, 8, 4 or 2; 0 = 16 */
+                              work"); 0 = 2 */
+    int32_t load_bytes;    /* cap on the weight load width: 32, 16, 8, 4 or 2;
+                              0 = 32 (one 256-bit load per lane) */
     int32_t pdl;           /* 1 = launch with programmatic dependent launch: the
                               kernel issues its first weight loads before waiting
                               for the previous kernel in the stream ([P5]

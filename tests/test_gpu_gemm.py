@@ -49,7 +49,7 @@ def test_columns_match_decode_gemv(w5):
     for n in range(8):
         y = wsw.gemv_bf16(Wd, X[n].float().cuda())
         rel = (Y[n] - y).norm() / y.norm()
-        assert rel.item() < 1e-5
+        assert rel.item() < 1e-4  # two fp32 sums in different orders, each within 1e-3 of fp64
 
 
 @pytest.mark.parametrize("M,K,N", [(1, 8, 1), (17, 24, 3), (130, 520, 9), (300, 1000, 40), (64, 4096, 129)])

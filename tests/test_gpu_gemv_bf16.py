@@ -48,7 +48,7 @@ def test_launch_knobs_are_bit_identical(M, K):
     Wd, xd = W.cuda(), x.cuda()
     ref = wsw.gemv_bf16(Wd, xd).clone()
     for rpw in (1, 2, 4):
-        for lb in (16, 8, 4, 2):
+        for lb in (32, 16, 8, 4, 2):
             for cps in (1, 2):
                 for pdl in (0, 1):
                     y = wsw.gemv_bf16(Wd, xd, opts=dict(rows_per_warp=rpw, load_bytes=lb, ctas_per_sm=cps, pdl=pdl))

@@ -80,7 +80,7 @@ def test_launch_knobs_and_padded_stride_bit_identical(orc, cfg2):
     Wqd, Wdd, xqd, xdd = _dev(Wq[:2000], Wd[:2000], xq, xd)
     ref = wsw.gemv_q8_0(Wqd, Wdd, xqd, xdd).clone()
     for rpw in (1, 2, 4):
-        for lb in (16, 8, 4):
+        for lb in (32, 16, 8, 4):
             for pdl in (0, 1):
                 y = wsw.gemv_q8_0(Wqd, Wdd, xqd, xdd, opts=dict(rows_per_warp=rpw, load_bytes=lb, pdl=pdl))
                 assert torch.equal(y.view(torch.int32), ref.view(torch.int32)), (rpw, lb, pdl)

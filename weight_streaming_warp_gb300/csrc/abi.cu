@@ -51,7 +51,7 @@ bool device_info(DeviceInfo *out, int *status) {
 }
 
 int resolve_opts(const wsw_launch_opts *o, Opts *out) {
-    Opts r{1, 16, false, 0};
+    Opts r{2, 32, false, 0};
     if (o) {
         if (o->rows_per_warp != 0) {
             if (o->rows_per_warp != 1 && o->rows_per_warp != 2 && o->rows_per_warp != 4)
@@ -59,8 +59,8 @@ int resolve_opts(const wsw_launch_opts *o, Opts *out) {
             r.rows_per_warp = o->rows_per_warp;
         }
         if (o->load_bytes != 0) {
-            if (o->load_bytes != 16 && o->load_bytes != 8 && o->load_bytes != 4 &&
-                o->load_bytes != 2)
+            if (o->load_bytes != 32 && o->load_bytes != 16 && o->load_bytes != 8 &&
+                o->load_bytes != 4 && o->load_bytes != 2)
                 return WSW_ERR_INVALID_ARG;
             r.load_bytes = o->load_bytes;
         }
@@ -93,7 +93,7 @@ cudaError_t ensure_smem(const void *kernel, int bytes) {
 
 int load_width(const void *base, int64_t pitch_bytes, int cap) {
     uint64_t a = reinterpret_cast<uint64_t>(base) | static_cast<uint64_t>(pitch_bytes);
-    int w = 16;
+    int w = 32;
     while (w > 2 && (a % static_cast<uint64_t>(w)) != 0) w >>= 1;
     return w < cap ? w : cap;
 }

@@ -34,6 +34,17 @@ template <int BYTES>
 struct StreamLoad;
 
 template <>
+struct StreamLoad<32> {
+    __device__ __forceinline__ static void run(const void *p, uint32_t *v, uint64_t pol) {
+        asm volatile(
+            "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+              "=r"(v[7])
+            : "l"(p), "l"(pol));
+    }
+};
+
+template <>
 struct StreamLoad<16> {
     __device__ __forceinline__ static void run(const void *p, uint32_t *v, uint64_t pol) {
         asm volatile(
@@ -94,6 +105,25 @@ __device__ __forceinline__ void load16(const void *p, uint32_t (&v)[4], uint64_t
     }
 }
 
+// Load 32 bytes of streamed data at p (32-byte aligned when LB == 32) as LB-byte
+// pieces; the eight words come out identical whatever LB is.
+template <int LB>
+__device__ __forceinline__ void load32(const void *p, uint32_t (&v)[8], uint64_t pol) {
+    if constexpr (LB == 32) {
+        StreamLoad<32>::run(p, v, pol);
+    } else {
+        const char *c = static_cast<const char *>(p);
+        uint32_t lo[4], hi[4];
+        load16<(LB > 16 ? 16 : LB)>(c, lo, pol);
+        load16<(LB > 16 ? 16 : LB)>(c + 16, hi, pol);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[i] = lo[i];
+            v[4 + i] = hi[i];
+        }
+    }
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -124,8 +154,8 @@ struct Opts {
 };
 int resolve_opts(const wsw_launch_opts *o, Opts *out);
 
-// The widest load width (16, 8, 4 or 2 bytes) that divides both the base address
-// and the row pitch in bytes, capped at `cap`.
+// The widest load width (32, 16, 8, 4 or 2 bytes) that divides both the base
+// address and the row pitch in bytes, capped at `cap`.
 int load_width(const void *base, int64_t pitch_bytes, int cap);
 
 // Raise a kernel's dynamic shared-memory limit to `bytes` once per device (later

@@ -11,41 +11,43 @@
 //   isum_b = sum_{i<32} Wq[r][32b+i] * xq[32b+i]   (exact int32).
 //
 // Canonical arithmetic (shared by the dense and the grouped kernels, which therefore
-// agree bit for bit): a lane owns 16-byte chunks, chunk 32*s + lane in step s of a
-// row; the two lanes of a block add their half sums with one shuffle; the even lane
-// multiplies the exact fp32 product Wd*xd by the block sum and accumulates it with an
-// fp32 FMA, blocks in increasing order; a xor-butterfly over the warp ends the row.
+// agree bit for bit): a lane owns whole blocks, block 32*s + lane in step s of a row
+// (one 256-bit load of 32 int8 values); the exact block sum comes from eight dp4a; the
+// lane multiplies the exact fp32 product Wd*xd by it and accumulates with an fp32 FMA,
+// its blocks in increasing order; at the end of each K-segment of two steps a
+// xor-butterfly reduces the lanes, and the segment sums are added first to last (the
+// work decomposition is in stream_gemv.cuh).
 #include <cuda_fp16.h>
 
-#include "common.cuh"
+#include "stream_gemv.cuh"
 
 namespace wsw {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kU = 4;  // row steps per register batch; two batches in flight
+constexpr int kWarps = sg::kWarps;
+constexpr int kThreads = sg::kThreads;
 
-__device__ __forceinline__ int dot16(const uint32_t (&w)[4], const uint4 &xv) {
-    int s = 0;
-    s = __dp4a(static_cast<int>(w[0]), static_cast<int>(xv.x), s);
-    s = __dp4a(static_cast<int>(w[1]), static_cast<int>(xv.y), s);
-    s = __dp4a(static_cast<int>(w[2]), static_cast<int>(xv.z), s);
-    s = __dp4a(static_cast<int>(w[3]), static_cast<int>(xv.w), s);
-    return s;
+__device__ __forceinline__ int dot32(const uint32_t (&w)[8], const uint4 &x0, const uint4 &x1) {
+    int s0 = 0, s1 = 0;
+    s0 = __dp4a(static_cast<int>(w[0]), static_cast<int>(x0.x), s0);
+    s1 = __dp4a(static_cast<int>(w[4]), static_cast<int>(x1.x), s1);
+    s0 = __dp4a(static_cast<int>(w[1]), static_cast<int>(x0.y), s0);
+    s1 = __dp4a(static_cast<int>(w[5]), static_cast<int>(x1.y), s1);
+    s0 = __dp4a(static_cast<int>(w[2]), static_cast<int>(x0.z), s0);
+    s1 = __dp4a(static_cast<int>(w[6]), static_cast<int>(x1.z), s1);
+    s0 = __dp4a(static_cast<int>(w[3]), static_cast<int>(x0.w), s0);
+    s1 = __dp4a(static_cast<int>(w[7]), static_cast<int>(x1.w), s1);
+    return s0 + s1;  // exact: |sum| <= 32 * 127 * 127
 }
 
-// One block's contribution: the pair's half sums are combined and the even lane
-// accumulates; odd lanes keep their accumulator unchanged (it stays 0).
-__device__ __forceinline__ float q8_accumulate(float acc, int half_sum, uint32_t wd_bits,
-                                               uint32_t xd_bits, int lane) {
-    const int isum = half_sum + __shfl_xor_sync(WSW_FULL_MASK, half_sum, 1);
-    if ((lane & 1) == 0) {
-        const float t = __half2float(__ushort_as_half(static_cast<unsigned short>(wd_bits))) *
-                        __half2float(__ushort_as_half(static_cast<unsigned short>(xd_bits)));
-        acc = fmaf(t, static_cast<float>(isum), acc);
-    }
-    return acc;
+__device__ __forceinline__ float half_bits(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// One block's contribution: (Wd * xd) is exact in fp32 (11 x 11 significant bits),
+// the block sum is exact in fp32 (< 2^24); one fused multiply-add.
+__device__ __forceinline__ float q8_accumulate(float acc, int isum, uint32_t wd_bits, uint32_t xd_bits) {
+    return fmaf(half_bits(wd_bits) * half_bits(xd_bits), static_cast<float>(isum), acc);
 }
 
 __device__ __forceinline__ float warp_sum(float s) {
@@ -56,152 +58,91 @@ __device__ __forceinline__ float warp_sum(float s) {
 
 // ---------------------------------------------------------------- dense ----
 
-struct Q8Args {
-    const int8_t *Wq;
-    const uint16_t *Wd;
-    int64_t M, K, ldq;
-    const int8_t *xq;
-    const uint16_t *xd;
-    float *y;
-    int64_t groups, per_warp, nsteps;  // nsteps = ceil(K / 512)
-};
-
-template <int R, int LB>
-__global__ void __launch_bounds__(kThreads, 2) gemv_q8_0_kernel(const Q8Args a) {
-    constexpr int U = kU / R;
-    extern __shared__ uint4 xs_q[];  // [nsteps * 32] chunks of xq, then xd as u16 [nsteps * 16]
-
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    const int64_t g0 = warp * a.per_warp;
-    int64_t g1 = g0 + a.per_warp;
-    if (g1 > a.groups) g1 = a.groups;
-    const int64_t T = g1 > g0 ? (g1 - g0) * a.nsteps : 0;
-    const int64_t nblk = a.K / 32;
-    const uint64_t pol = policy_evict_first();
-
-    uint32_t wA[U][R][4], wB[U][R][4];
-    uint32_t dA[U][R], dB[U][R];
-    int64_t it = 0, ig = g0, is = 0;
-
-    auto issue = [&](uint32_t(&w)[U][R][4], uint32_t(&d)[U][R]) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (it < T) {
-                const int64_t c = is * 32 + lane;
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int64_t row = ig * R + r;
-                    d[u][r] = 0u;
-                    if (row < a.M && 16 * c < a.K) {
-                        load16<LB>(a.Wq + row * a.ldq + 16 * c, w[u][r], pol);
-                        if ((lane & 1) == 0) StreamLoad<2>::run(a.Wd + row * nblk + (c >> 1), &d[u][r], pol);
-                    } else {
-                        w[u][r][0] = w[u][r][1] = w[u][r][2] = w[u][r][3] = 0u;
-                    }
-                }
-                ++it;
-                if (++is == a.nsteps) { is = 0; ++ig; }
-            }
-        }
+struct Q8 {
+    static constexpr int kStepElems = 1024;
+    static constexpr bool kGlobalX = false;  // x is always staged in shared memory
+    struct Args {
+        sg::Common c;
+        const int8_t *Wq;
+        const uint16_t *Wd;
+        int64_t K, ldq;
+        const int8_t *xq;
+        const uint16_t *xd;
+        float *y;
     };
+    struct Buf { uint32_t w[8]; uint32_t d; };
+    struct Acc { float a; };
+    struct XVal { uint4 x0, x1; uint32_t d; };
 
-    issue(wA, dA);
-    if (T > 0) {
+    template <int LB>
+    __device__ __forceinline__ static void load(const Args &a, int64_t row, int step, int lane, Buf &b,
+                                                uint64_t pol) {
+        const int64_t blk = static_cast<int64_t>(step) * 32 + lane;
+        b.d = 0u;
+        if (32 * blk < a.K) {
+            load32<LB>(a.Wq + row * a.ldq + 32 * blk, b.w, pol);
+            StreamLoad<2>::run(a.Wd + row * (a.K / 32) + blk, &b.d, pol);
+        } else {
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int64_t row = g0 * R + r;
-            if (row < a.M) {
-                const char *p = reinterpret_cast<const char *>(a.Wq + row * a.ldq);
-                int64_t nbytes = a.K;
-                if (nbytes > 16384 / R) nbytes = 16384 / R;
-                for (int64_t off = 4096 / R + lane * 128; off < nbytes; off += 32 * 128) prefetch_l2(p + off);
-            }
+            for (int i = 0; i < 8; ++i) b.w[i] = 0u;
         }
     }
-
-    pdl_wait();
-    {
-        const int64_t nchunks = a.nsteps * 32;
-        uint16_t *xs_d = reinterpret_cast<uint16_t *>(xs_q + nchunks);
+    __device__ __forceinline__ static void zero(Buf &b) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b.w[i] = 0u;
+        b.d = 0u;
+    }
+    __device__ __forceinline__ static void prefetch(const Args &a, int64_t row, int step, int lane) {
+        const char *p = reinterpret_cast<const char *>(a.Wq + row * a.ldq);
+        const int64_t end = a.K;
+        int64_t begin = static_cast<int64_t>(step) * 1024 + 4096;
+        for (int64_t off = begin + lane * 128; off < end && off < begin + 8192; off += 32 * 128) prefetch_l2(p + off);
+    }
+    // Shared memory: xq as two planes of 16-byte halves [2][nsteps * 32], then xd.
+    template <bool XS>
+    __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
+        uint4 *xs = reinterpret_cast<uint4 *>(xsm);
+        const int64_t nslots = static_cast<int64_t>(nsteps) * 32;
+        uint16_t *xs_d = reinterpret_cast<uint16_t *>(xs + 2 * nslots);
+        const int64_t nblk = a.K / 32;
         const bool xvec = (reinterpret_cast<uintptr_t>(a.xq) & 15) == 0;
-        for (int64_t c = threadIdx.x; c < nchunks; c += kThreads) {
+        for (int64_t h = threadIdx.x; h < 2 * nslots; h += sg::kThreads) {
+            // half h = bytes 16h .. 16h+15 = plane (h & 1) of block h >> 1
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (16 * c < a.K) {
+            if (16 * h < a.K) {
                 if (xvec) {
-                    v = __ldg(reinterpret_cast<const uint4 *>(a.xq) + c);
+                    v = __ldg(reinterpret_cast<const uint4 *>(a.xq) + h);
                 } else {
                     uint32_t t[4] = {0u, 0u, 0u, 0u};
                     for (int i = 0; i < 16; ++i)
-                        t[i >> 2] |= (static_cast<uint32_t>(static_cast<uint8_t>(a.xq[16 * c + i])) << (8 * (i & 3)));
+                        t[i >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(a.xq[16 * h + i])) << (8 * (i & 3));
                     v = make_uint4(t[0], t[1], t[2], t[3]);
                 }
             }
-            xs_q[c] = v;
+            xs[(h & 1) * nslots + (h >> 1)] = v;
         }
-        for (int64_t b = threadIdx.x; b < a.nsteps * 16; b += kThreads) xs_d[b] = b < nblk ? a.xd[b] : 0;
-        __syncthreads();
+        for (int64_t b = threadIdx.x; b < nslots; b += sg::kThreads) xs_d[b] = b < nblk ? a.xd[b] : 0;
     }
-    pdl_launch_dependents();
-    const uint16_t *xs_d = reinterpret_cast<const uint16_t *>(xs_q + a.nsteps * 32);
-
-    float acc[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = 0.0f;
-    int64_t ct = 0, cg = g0, cs = 0;
-
-    auto compute = [&](const uint32_t(&w)[U][R][4], const uint32_t(&d)[U][R]) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (ct < T) {
-                const int64_t c = cs * 32 + lane;
-                const uint4 xv = xs_q[c];
-                const uint32_t xdb = xs_d[c >> 1];
-#pragma unroll
-                for (int r = 0; r < R; ++r) acc[r] = q8_accumulate(acc[r], dot16(w[u][r], xv), d[u][r], xdb, lane);
-                ++ct;
-                if (++cs == a.nsteps) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const float s = warp_sum(acc[r]);
-                        const int64_t row = cg * R + r;
-                        if (lane == r && row < a.M) a.y[row] = s;
-                        acc[r] = 0.0f;
-                    }
-                    cs = 0;
-                    ++cg;
-                }
-            }
-        }
-    };
-
-    while (ct < T) {
-        issue(wB, dB);
-        compute(wA, dA);
-        if (ct >= T) break;
-        issue(wA, dA);
-        compute(wB, dB);
+    template <bool XS>
+    __device__ __forceinline__ static XVal load_x(const Args &, const unsigned char *xsm, int step, int lane,
+                                                  int nsteps) {
+        const uint4 *xs = reinterpret_cast<const uint4 *>(xsm);
+        const int64_t nslots = static_cast<int64_t>(nsteps) * 32;
+        const uint16_t *xs_d = reinterpret_cast<const uint16_t *>(xs + 2 * nslots);
+        const int64_t b = static_cast<int64_t>(step) * 32 + lane;
+        XVal v;
+        v.x0 = xs[b];
+        v.x1 = xs[nslots + b];
+        v.d = xs_d[b];
+        return v;
     }
-}
-
-template <int R, int LB>
-cudaError_t launch_q8(const Q8Args &a, unsigned ctas, size_t smem, cudaStream_t s, bool pdl) {
-    if (smem > 48 * 1024) {
-        cudaError_t e = ensure_smem(reinterpret_cast<const void *>(gemv_q8_0_kernel<R, LB>), static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
+    __device__ __forceinline__ static void clear(Acc &c) { c.a = 0.0f; }
+    __device__ __forceinline__ static void accumulate(Acc &c, const Buf &b, const XVal &x) {
+        c.a = q8_accumulate(c.a, dot32(b.w, x.x0, x.x1), b.d, x.d);
     }
-    return launch(gemv_q8_0_kernel<R, LB>, dim3(ctas), dim3(kThreads), smem, s, pdl, a);
-}
-
-template <int R>
-cudaError_t launch_q8_lb(int lb, const Q8Args &a, unsigned ctas, size_t smem, cudaStream_t s, bool pdl) {
-    switch (lb) {
-        case 16: return launch_q8<R, 16>(a, ctas, smem, s, pdl);
-        case 8: return launch_q8<R, 8>(a, ctas, smem, s, pdl);
-        case 4: return launch_q8<R, 4>(a, ctas, smem, s, pdl);
-        default: return launch_q8<R, 2>(a, ctas, smem, s, pdl);
-    }
-}
+    __device__ __forceinline__ static float lane_total(const Acc &c) { return c.a; }
+    __device__ __forceinline__ static void store(const Args &a, int64_t row, float s) { a.y[row] = s; }
+};
 
 // ---------------------------------------------------------------- grouped ---
 
@@ -220,6 +161,7 @@ struct MoeArgs {
     float *y;
     int32_t *err;
     int64_t nsteps;
+    int seg_steps;  // as the dense kernel on one expert's Mo x K matrix
 };
 
 // Shared memory: cnt[E], off[E], cur[E], used[E], list[R], nused.
@@ -232,7 +174,6 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gemv_q8_0_kernel(const MoeArg
     int *used = cur + a.E;
     int *list = used + a.E;
     __shared__ int s_nused;
-    __shared__ int s_warp_tot[kWarps];
 
     pdl_wait();  // ids and the activation come from earlier kernels
     pdl_launch_dependents();
@@ -275,7 +216,6 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gemv_q8_0_kernel(const MoeArg
         const int e = a.ids[m];
         if (e >= 0 && e < a.E) list[off[e] + atomicAdd(&cur[e], 1)] = static_cast<int>(m);
     }
-    (void)s_warp_tot;
     __syncthreads();
 
     // Flattened (used expert, output row) work, split evenly over the grid's warps.
@@ -299,46 +239,56 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gemv_q8_0_kernel(const MoeArg
         const uint16_t *drow = a.Wd + (static_cast<int64_t>(e) * a.Mo + o) * nblk;
         for (int t0 = 0; t0 < ntok; t0 += kMoeNT) {
             int m[kMoeNT];
-            float acc[kMoeNT];
+            float acc[kMoeNT], total[kMoeNT];
 #pragma unroll
             for (int j = 0; j < kMoeNT; ++j) {
                 m[j] = (t0 + j < ntok) ? toks[t0 + j] : -1;
                 acc[j] = 0.0f;
+                total[j] = 0.0f;
             }
-            for (int64_t s = 0; s < a.nsteps; ++s) {
-                const int64_t c = s * 32 + lane;
-                uint32_t w[4] = {0u, 0u, 0u, 0u};
+            for (int s = 0; s < a.nsteps; ++s) {
+                const int64_t b = static_cast<int64_t>(s) * 32 + lane;
+                uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
                 uint32_t db = 0u;
-                const bool valid = 16 * c < a.K;
+                const bool valid = b < nblk;
                 if (valid) {
-                    load16<LB>(wrow + 16 * c, w, pol);
-                    if ((lane & 1) == 0) StreamLoad<2>::run(drow + (c >> 1), &db, pol);
+                    load32<LB>(wrow + 32 * b, w, pol);
+                    StreamLoad<2>::run(drow + b, &db, pol);
                 }
+                // a K-segment ends after this step: reduce and add, first to last
+                const bool seg_end = ((s + 1) % a.seg_steps == 0) || (s + 1 == a.nsteps);
+                const int seg = s / a.seg_steps;
 #pragma unroll
                 for (int j = 0; j < kMoeNT; ++j) {
                     if (m[j] < 0) continue;  // warp-uniform
-                    uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+                    uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
                     uint32_t xdb = 0u;
                     if (valid) {
-                        const int8_t *xr = a.xq + static_cast<int64_t>(m[j]) * a.K + 16 * c;
+                        const int8_t *xr = a.xq + static_cast<int64_t>(m[j]) * a.K + 32 * b;
                         if ((reinterpret_cast<uintptr_t>(xr) & 15) == 0) {
-                            xv = __ldg(reinterpret_cast<const uint4 *>(xr));
+                            x0 = __ldg(reinterpret_cast<const uint4 *>(xr));
+                            x1 = __ldg(reinterpret_cast<const uint4 *>(xr) + 1);
                         } else {
-                            uint32_t t[4] = {0u, 0u, 0u, 0u};
-                            for (int i = 0; i < 16; ++i)
+                            uint32_t t[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                            for (int i = 0; i < 32; ++i)
                                 t[i >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(xr[i])) << (8 * (i & 3));
-                            xv = make_uint4(t[0], t[1], t[2], t[3]);
+                            x0 = make_uint4(t[0], t[1], t[2], t[3]);
+                            x1 = make_uint4(t[4], t[5], t[6], t[7]);
                         }
-                        xdb = __ldg(a.xd + static_cast<int64_t>(m[j]) * nblk + (c >> 1));
+                        xdb = __ldg(a.xd + static_cast<int64_t>(m[j]) * nblk + b);
                     }
-                    acc[j] = q8_accumulate(acc[j], dot16(w, xv), db, xdb, lane);
+                    acc[j] = q8_accumulate(acc[j], dot32(w, x0, x1), db, xdb);
+                    if (seg_end) {
+                        const float p = warp_sum(acc[j]);
+                        total[j] = seg == 0 ? p : total[j] + p;
+                        acc[j] = 0.0f;
+                    }
                 }
             }
 #pragma unroll
             for (int j = 0; j < kMoeNT; ++j) {
                 if (m[j] < 0) continue;
-                const float sum = warp_sum(acc[j]);
-                if (lane == 0) a.y[static_cast<int64_t>(m[j]) * a.Mo + o] = sum;
+                if (lane == 0) a.y[static_cast<int64_t>(m[j]) * a.Mo + o] = total[j];
             }
         }
     }
@@ -368,28 +318,19 @@ extern "C" int wsw_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, in
     if (K == 0)
         return cudaMemsetAsync(y, 0, static_cast<size_t>(M) * 4, s) == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
 
-    Q8Args a;
-    a.Wq = Wq; a.Wd = Wd; a.M = M; a.K = K; a.ldq = ldq; a.xq = xq; a.xd = xd; a.y = y;
     const int R = o.rows_per_warp;
-    a.groups = (M + R - 1) / R;
-    a.nsteps = (K + 511) / 512;
+    const int64_t nsteps = (K + Q8::kStepElems - 1) / Q8::kStepElems;
+    if (nsteps > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
+    Q8::Args a;
+    a.c = sg::make_common(M, static_cast<int>(nsteps), R, di.sm_count);
+    if (static_cast<int64_t>(a.c.nseg) * R > sg::kMaxPartials) return WSW_ERR_UNSUPPORTED;
+    a.Wq = Wq; a.Wd = Wd; a.K = K; a.ldq = ldq; a.xq = xq; a.xd = xd; a.y = y;
     const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 2;
-    const int64_t target = static_cast<int64_t>(di.sm_count) * cps * kWarps;
-    a.per_warp = (a.groups + target - 1) / target;
-    const int64_t warps = (a.groups + a.per_warp - 1) / a.per_warp;
-    const unsigned ctas = static_cast<unsigned>((warps + kWarps - 1) / kWarps);
-    const size_t smem = static_cast<size_t>(a.nsteps) * (512 + 32);
-    if (smem > 48 * 1024) {
-        // Large K: allow more dynamic shared memory (up to the device's opt-in limit).
-        if (smem > static_cast<size_t>(di.max_smem_optin)) return WSW_ERR_UNSUPPORTED;
-    }
+    const unsigned ctas = static_cast<unsigned>(di.sm_count * cps);
+    const size_t x_smem = static_cast<size_t>(nsteps) * (1024 + 64);
+    if (sg::kMaxPartials * 4 + x_smem > static_cast<size_t>(di.max_smem_optin)) return WSW_ERR_UNSUPPORTED;
     const int lb = load_width(Wq, ldq, o.load_bytes);
-    cudaError_t e = cudaSuccess;
-    switch (R) {
-        case 1: e = launch_q8_lb<1>(lb, a, ctas, smem, s, o.pdl); break;
-        case 2: e = launch_q8_lb<2>(lb, a, ctas, smem, s, o.pdl); break;
-        default: e = launch_q8_lb<4>(lb, a, ctas, smem, s, o.pdl); break;
-    }
+    const cudaError_t e = sg::launch_stream_gemv<Q8>(R, lb, true, a, ctas, x_smem, s, o.pdl);
     return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
 }
 
@@ -416,7 +357,8 @@ extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E
     MoeArgs a;
     a.Wq = Wq; a.Wd = Wd; a.E = E; a.Mo = Mo; a.K = K; a.xq = xq; a.xd = xd; a.ids = ids; a.R = R;
     a.y = y; a.err = err_flag;
-    a.nsteps = (K + 511) / 512;
+    a.nsteps = (K + Q8::kStepElems - 1) / Q8::kStepElems;
+    a.seg_steps = sg::choose_seg_steps(Mo, static_cast<int>(a.nsteps), di.sm_count);
     const size_t smem = static_cast<size_t>(4 * E + R) * sizeof(int);
     const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 2;
     const unsigned ctas = static_cast<unsigned>(di.sm_count * cps);
@@ -431,6 +373,7 @@ extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E
     };
     cudaError_t e;
     switch (lb) {
+        case 32: e = run(moe_gemv_q8_0_kernel<32>); break;
         case 16: e = run(moe_gemv_q8_0_kernel<16>); break;
         case 8: e = run(moe_gemv_q8_0_kernel<8>); break;
         case 4: e = run(moe_gemv_q8_0_kernel<4>); break;
