@@ -333,6 +333,81 @@ def measure_chain(torch, wsw, dev):
     return res
 
 
+def _graph_rate(torch, fn, n, reps=5):
+    """Median seconds per call of fn(stream) captured n times in one graph."""
+    def body(stream):
+        for _ in range(n):
+            fn(stream)
+    g = _graph(torch, body)
+    _time_graph(torch, g, 2)
+    return statistics.median(_time_graph(torch, g, 1) for _ in range(reps)) / n
+
+
+def measure_rows(torch, wsw, dev):
+    """The other hot-path calls on their configured shapes (graph-amortised, inputs
+    rotating over copies larger than L2 where a single copy would fit)."""
+    import weight_streaming_warp_gb300.synthetic as syn
+    g = torch.Generator(device=dev)
+    g.manual_seed(2)
+    out = {}
+    # small-batch prefill GEMM, W 2560 x 10240 (packed and one-line padded rows)
+    Mg, Kg = 2560, 10240
+    Ws = [torch.randn((Mg, Kg), generator=g, device=dev).mul_(0.02).to(torch.bfloat16) for _ in range(12)]
+    for ld in (Kg, Kg + 64):
+        Wl = Ws if ld == Kg else [wsw.upload_padded(w, ld) for w in Ws]
+        for N in (8, 128, 512):
+            X = torch.randn((N, Kg), generator=g, device=dev).to(torch.bfloat16)
+            Y = torch.empty((N, Mg), dtype=torch.float32, device=dev)
+            it = [0]
+
+            def fn(stream, X=X, Y=Y, Wl=Wl):
+                wsw.gemm_bf16(Wl[it[0] % len(Wl)], X, out=Y)
+                it[0] += 1
+            t = _graph_rate(torch, fn, 24)
+            key = "gemm_bf16_N%d_%s" % (N, "packed" if ld == Kg else "padded")
+            out[key] = {"us": round(t * 1e6, 2), "TFLOPs": round(2.0 * N * Mg * Kg / t / 1e12, 2),
+                        "GBps": round((Mg * Kg * 2 + N * Kg * 2 + N * Mg * 4) / t / 1e9, 1)}
+        del Wl
+    del Ws
+    # q8_0 KV cache dequant, 4 heads x 128
+    for depth in (32768, 65536):
+        copies = 8
+        qs = [torch.randint(-127, 128, (depth, 4, 128), dtype=torch.int8, device=dev, generator=g) for _ in range(copies)]
+        ds = [torch.rand((depth, 4, 4), device=dev, generator=g).half() for _ in range(copies)]
+        o = torch.empty((4, depth, 128), dtype=torch.float16, device=dev)
+        it = [0]
+
+        def fn(stream, qs=qs, ds=ds, o=o):
+            i = it[0] % copies
+            wsw.dequant_q8_0_kv(qs[i], ds[i], out=o)
+            it[0] += 1
+        t = _graph_rate(torch, fn, 32)
+        nb = depth * 4 * 128 * (1 + 2) + depth * 4 * 4 * 2
+        out["dequant_kv_d%d" % depth] = {"us": round(t * 1e6, 2), "GBps": round(nb / t / 1e9, 1)}
+        del qs, ds
+    # grouped MoE mat-vec (gate_up: 1536 x 2048 per expert), 128 experts, top-8
+    E, Mo, Km = 128, 1536, 2048
+    Wq = torch.randint(-127, 128, (E, Mo, Km), dtype=torch.int8, device=dev, generator=g)
+    Wd = (torch.rand((E, Mo, Km // 32), device=dev, generator=g) * 1e-3).half()
+    for T in (1, 16, 512):
+        ids = syn.routing(0, "bench_route%d" % T, T, E, 8).to(dev)
+        R = T * 8
+        xq = torch.randint(-127, 128, (R, Km), dtype=torch.int8, device=dev, generator=g)
+        xd = torch.rand((R, Km // 32), device=dev, generator=g).half()
+        y = torch.empty((R, Mo), dtype=torch.float32, device=dev)
+
+        def fn(stream, ids=ids, xq=xq, xd=xd, y=y):
+            wsw.moe_gemv_q8_0(Wq, Wd, xq, xd, ids, out=y)
+        t = _graph_rate(torch, fn, 8 if T == 512 else 32)
+        used = len(set(ids.tolist()))
+        nb = used * (Mo * Km + Mo * Km // 16) + R * (Km + Km // 16) + R * Mo * 4
+        out["moe_gate_up_T%d" % T] = {"us": round(t * 1e6, 2), "experts_used": used, "GBps": round(nb / t / 1e9, 1),
+                                     "note": "weights of the used experts once + activations + y"}
+    del Wq, Wd
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_e2e(torch, wl, dev, steps):
     """Through the C ABI with host buffers: per step, copy the batch's activations
     from pinned host memory, launch every token, copy y back."""
@@ -450,6 +525,7 @@ def run_ours(args):
     e2e = measure_e2e(torch, wl, dev, args.steps)
     del step_graph
     chain = measure_chain(torch, wsw, dev) if rank == 0 else None
+    rows = measure_rows(torch, wsw, dev) if rank == 0 else None
 
     if pg:
         pg.barrier()
@@ -489,6 +565,7 @@ def run_ours(args):
                      "launch_us": {"median": round(k_med * 1e6, 3), "min": round(k_min * 1e6, 3),
                                    "max": round(k_max * 1e6, 3)}},
         "chain_27b_bf16": chain,
+        "rows": rows,
         "e2e": e2e,
         "gpu_launches": 4 * TOKENS * args.steps,
         "clocks": clk,

@@ -117,3 +117,26 @@ def test_empty_and_single_row():
                           torch.zeros((0, 1), dtype=torch.float16, device="cuda"),
                           torch.zeros(0, dtype=torch.int32, device="cuda"))
     assert y.numel() == 0
+
+
+def test_every_output_written_and_equal_to_dense(orc):
+    """Experts with many rows (several token batches): every y entry is written, and
+    sampled rows equal the dense mat-vec on their expert bit for bit."""
+    wsw = need_gpu()
+    En, Mo, K, T = 16, 256, 512, 128
+    g = np.random.default_rng(11)
+    Wq = g.integers(-127, 128, size=(En, Mo, K)).astype(np.int8)
+    Wd = g.integers(0x0800, 0x1c00, size=(En, Mo, K // 32)).astype(np.uint16)
+    ids = syn.routing(3, "dense_many", T, En, TOPK).numpy()
+    R = T * TOPK
+    xq = g.integers(-127, 128, size=(R, K)).astype(np.int8)
+    xd = g.integers(0x0800, 0x1c00, size=(R, K // 32)).astype(np.uint16)
+    y = torch.full((R, Mo), float("nan"), device="cuda")
+    Wqd, Wdd = torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda()
+    wsw.moe_gemv_q8_0(Wqd, Wdd, torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda(),
+                      torch.from_numpy(ids).cuda(), out=y)
+    assert not torch.isnan(y).any()
+    for m in np.random.default_rng(0).integers(0, R, 24):
+        e = ids[m]
+        yd = wsw.gemv_q8_0(Wqd[e], Wdd[e], torch.from_numpy(xq[m]).cuda(), u16_to_torch(xd[m], torch.float16).cuda())
+        assert torch.equal(yd.view(torch.int32), y[m].view(torch.int32)), m

@@ -145,8 +145,19 @@ struct Q8 {
 };
 
 // ---------------------------------------------------------------- grouped ---
+//
+// Every CTA buckets the rows by expert in shared memory (counts, exclusive scan,
+// scatter; no global scratch).  An expert's rows are cut into token batches of up to
+// kMoeNT rows; the work units are (used expert, output row o, token batch j), ordered
+// expert by expert, then by o, then by j, so the batches of one weight row follow each
+// other and re-read that row from L2.  Units are split evenly over all warps of the
+// grid; each warp streams its units with two register batches of weight loads in
+// flight, like the dense kernel, and for each token of a unit follows the dense
+// kernel's arithmetic exactly (lane blocks, K-segments of the dense kernel on an
+// Mo x K matrix, butterfly, segments added in order).
 
-constexpr int kMoeNT = 4;         // tokens of one expert per pass over a weight row
+constexpr int kMoeNT = 4;         // rows of one expert per pass over a weight row
+constexpr int kMoeU = 4;          // steps per register batch
 constexpr int kMoeMaxE = 1024;
 constexpr int kMoeMaxR = 16384;
 
@@ -160,25 +171,27 @@ struct MoeArgs {
     int64_t R;
     float *y;
     int32_t *err;
-    int64_t nsteps;
+    int nsteps;     // ceil(K / 1024)
     int seg_steps;  // as the dense kernel on one expert's Mo x K matrix
 };
 
-// Shared memory: cnt[E], off[E], cur[E], used[E], list[R], nused.
+// Shared memory: cnt[E], off[E], cur[E], nbt[E] (token batches), ubase[E+1] (first
+// unit of each used expert, int64), used[E], list[R].
 template <int LB>
 __global__ void __launch_bounds__(kThreads, 2) moe_gemv_q8_0_kernel(const MoeArgs a) {
     extern __shared__ int moe_smem[];
     int *cnt = moe_smem;
     int *off = cnt + a.E;
     int *cur = off + a.E;
-    int *used = cur + a.E;
+    int *nbt = cur + a.E;
+    int64_t *ubase = reinterpret_cast<int64_t *>(nbt + a.E);  // 16 E bytes in: 8-byte aligned
+    int *used = reinterpret_cast<int *>(ubase + a.E + 1);
     int *list = used + a.E;
     __shared__ int s_nused;
 
     pdl_wait();  // ids and the activation come from earlier kernels
     pdl_launch_dependents();
 
-    // Bucket the rows by expert (every CTA does this for itself; no global scratch).
     for (int64_t e = threadIdx.x; e < a.E; e += kThreads) { cnt[e] = 0; cur[e] = 0; }
     __syncthreads();
     bool bad = false;
@@ -190,107 +203,197 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gemv_q8_0_kernel(const MoeArg
     if (bad && blockIdx.x == 0 && a.err) atomicOr(a.err, 1);
     __syncthreads();
     if (threadIdx.x < 32) {
-        // Exclusive scan of cnt and compaction of the used experts, in expert order.
+        // Exclusive scans (rows, units) and the list of used experts, in expert order.
         int run = 0, urun = 0;
+        int64_t unit_run = 0;
         for (int64_t base = 0; base < a.E; base += 32) {
             const int64_t e = base + threadIdx.x;
             const int c = e < a.E ? cnt[e] : 0;
+            const int nb = (c + kMoeNT - 1) / kMoeNT;
             int incl = c, uincl = c > 0;
+            int64_t units = static_cast<int64_t>(nb) * a.Mo, uninc = units;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int t = __shfl_up_sync(WSW_FULL_MASK, incl, o);
                 const int ut = __shfl_up_sync(WSW_FULL_MASK, uincl, o);
-                if (threadIdx.x >= o) { incl += t; uincl += ut; }
+                const int64_t nt = __shfl_up_sync(WSW_FULL_MASK, uninc, o);
+                if (threadIdx.x >= o) { incl += t; uincl += ut; uninc += nt; }
             }
             if (e < a.E) {
                 off[e] = run + incl - c;
-                if (c > 0) used[urun + uincl - 1] = static_cast<int>(e);
+                nbt[e] = nb;
+                if (c > 0) {
+                    used[urun + uincl - 1] = static_cast<int>(e);
+                    ubase[urun + uincl - 1] = unit_run + uninc - units;
+                }
             }
             run += __shfl_sync(WSW_FULL_MASK, incl, 31);
             urun += __shfl_sync(WSW_FULL_MASK, uincl, 31);
+            unit_run += __shfl_sync(WSW_FULL_MASK, uninc, 31);
         }
-        if (threadIdx.x == 0) s_nused = urun;
+        if (threadIdx.x == 0) {
+            s_nused = urun;
+            ubase[urun] = unit_run;
+        }
     }
     __syncthreads();
-    for (int64_t m = threadIdx.x; m < a.R; m += kThreads) {
-        const int e = a.ids[m];
-        if (e >= 0 && e < a.E) list[off[e] + atomicAdd(&cur[e], 1)] = static_cast<int>(m);
+    // Stable scatter by warp 0: rows enter their expert's list in row order, so every
+    // CTA builds the same list and the token batches (expert, row, j) that different
+    // CTAs take are the same sets of rows.
+    if (threadIdx.x < 32) {
+        const int lane0 = threadIdx.x;
+        for (int64_t base = 0; base < a.R; base += 32) {
+            const int64_t m = base + lane0;
+            const int e = m < a.R ? a.ids[m] : -1;
+            const bool valid = e >= 0 && e < a.E;
+            const int key = valid ? e : static_cast<int>(a.E) + lane0;  // invalid rows never group
+            const unsigned peers = __match_any_sync(WSW_FULL_MASK, key);
+            const int rank = __popc(peers & ((1u << lane0) - 1u));
+            if (valid) list[off[e] + cur[e] + rank] = static_cast<int>(m);
+            __syncwarp();
+            if (valid && lane0 == __ffs(peers) - 1) cur[e] += __popc(peers);
+            __syncwarp();
+        }
     }
     __syncthreads();
 
-    // Flattened (used expert, output row) work, split evenly over the grid's warps.
     const int lane = threadIdx.x & 31;
+    const int nused = s_nused;
+    const int64_t total = ubase[nused];
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
     const int64_t warp = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    const int64_t total = static_cast<int64_t>(s_nused) * a.Mo;
-    const int64_t per = (total + nwarps - 1) / nwarps;
-    int64_t w0 = warp * per, w1 = w0 + per;
-    if (w1 > total) w1 = total;
+    const int64_t w0 = warp * total / nwarps, w1 = (warp + 1) * total / nwarps;
+    if (w0 >= w1) return;
+    const int nsteps = a.nsteps;
     const int64_t nblk = a.K / 32;
     const uint64_t pol = policy_evict_first();
 
-    for (int64_t item = w0; item < w1; ++item) {
-        const int64_t u = item / a.Mo;
-        const int64_t o = item - u * a.Mo;
-        const int e = used[u];
-        const int ntok = cnt[e];
-        const int *toks = list + off[e];
-        const int8_t *wrow = a.Wq + (static_cast<int64_t>(e) * a.Mo + o) * a.K;
-        const uint16_t *drow = a.Wd + (static_cast<int64_t>(e) * a.Mo + o) * nblk;
-        for (int t0 = 0; t0 < ntok; t0 += kMoeNT) {
-            int m[kMoeNT];
-            float acc[kMoeNT], total[kMoeNT];
-#pragma unroll
-            for (int j = 0; j < kMoeNT; ++j) {
-                m[j] = (t0 + j < ntok) ? toks[t0 + j] : -1;
-                acc[j] = 0.0f;
-                total[j] = 0.0f;
-            }
-            for (int s = 0; s < a.nsteps; ++s) {
-                const int64_t b = static_cast<int64_t>(s) * 32 + lane;
-                uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                uint32_t db = 0u;
-                const bool valid = b < nblk;
-                if (valid) {
-                    load32<LB>(wrow + 32 * b, w, pol);
-                    StreamLoad<2>::run(drow + b, &db, pol);
+    // locate the first unit: used expert index by binary search over ubase
+    int lo = 0, hi = nused - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ubase[mid] <= w0) lo = mid; else hi = mid - 1;
+    }
+    struct Cursor {
+        int ui;      // used-expert index
+        int e, nb;   // expert, its token batches
+        int64_t o;   // output row
+        int j;       // token batch
+        int st;      // step
+    };
+    Cursor ic;
+    {
+        const int64_t r = w0 - ubase[lo];
+        ic.ui = lo; ic.e = used[lo]; ic.nb = nbt[ic.e];
+        ic.o = r / ic.nb; ic.j = static_cast<int>(r - ic.o * ic.nb); ic.st = 0;
+    }
+    Cursor cc = ic;
+    int64_t iu = w0, cu = w0;
+    auto advance = [&](Cursor &c) {
+        if (++c.st == nsteps) {
+            c.st = 0;
+            if (++c.j == c.nb) {
+                c.j = 0;
+                if (++c.o == a.Mo) {
+                    c.o = 0;
+                    if (++c.ui < nused) { c.e = used[c.ui]; c.nb = nbt[c.e]; }
                 }
-                // a K-segment ends after this step: reduce and add, first to last
-                const bool seg_end = ((s + 1) % a.seg_steps == 0) || (s + 1 == a.nsteps);
+            }
+            return true;
+        }
+        return false;
+    };
+
+    uint32_t wA[kMoeU][8], wB[kMoeU][8], dA[kMoeU], dB[kMoeU];
+    auto issue = [&](uint32_t(&w)[kMoeU][8], uint32_t(&d)[kMoeU]) {
+#pragma unroll
+        for (int u = 0; u < kMoeU; ++u) {
+            if (iu < w1) {
+                const int64_t b = static_cast<int64_t>(ic.st) * 32 + lane;
+                const int64_t row = static_cast<int64_t>(ic.e) * a.Mo + ic.o;
+                d[u] = 0u;
+                if (b < nblk) {
+                    load32<LB>(a.Wq + row * a.K + 32 * b, w[u], pol);
+                    StreamLoad<2>::run(a.Wd + row * nblk + b, &d[u], pol);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) w[u][i] = 0u;
+                }
+                if (advance(ic)) ++iu;
+            }
+        }
+    };
+
+    int m[kMoeNT];
+    float acc[kMoeNT], tot[kMoeNT];
+    auto load_tokens = [&]() {
+        const int base = off[cc.e] + cc.j * kMoeNT;
+        const int left = cnt[cc.e] - cc.j * kMoeNT;
+#pragma unroll
+        for (int t = 0; t < kMoeNT; ++t) {
+            m[t] = t < left ? list[base + t] : -1;
+            acc[t] = 0.0f;
+            tot[t] = 0.0f;
+        }
+    };
+    load_tokens();
+    auto compute = [&](const uint32_t(&w)[kMoeU][8], const uint32_t(&d)[kMoeU]) {
+#pragma unroll
+        for (int u = 0; u < kMoeU; ++u) {
+            if (cu < w1) {
+                const int s = cc.st;
+                const int64_t b = static_cast<int64_t>(s) * 32 + lane;
+                const bool valid = b < nblk;
+                const bool seg_end = ((s + 1) % a.seg_steps == 0) || (s + 1 == nsteps);
                 const int seg = s / a.seg_steps;
 #pragma unroll
-                for (int j = 0; j < kMoeNT; ++j) {
-                    if (m[j] < 0) continue;  // warp-uniform
+                for (int t = 0; t < kMoeNT; ++t) {
+                    if (m[t] < 0) continue;  // warp-uniform
                     uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
                     uint32_t xdb = 0u;
                     if (valid) {
-                        const int8_t *xr = a.xq + static_cast<int64_t>(m[j]) * a.K + 32 * b;
+                        const int8_t *xr = a.xq + static_cast<int64_t>(m[t]) * a.K + 32 * b;
                         if ((reinterpret_cast<uintptr_t>(xr) & 15) == 0) {
                             x0 = __ldg(reinterpret_cast<const uint4 *>(xr));
                             x1 = __ldg(reinterpret_cast<const uint4 *>(xr) + 1);
                         } else {
-                            uint32_t t[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                            uint32_t tt[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
                             for (int i = 0; i < 32; ++i)
-                                t[i >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(xr[i])) << (8 * (i & 3));
-                            x0 = make_uint4(t[0], t[1], t[2], t[3]);
-                            x1 = make_uint4(t[4], t[5], t[6], t[7]);
+                                tt[i >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(xr[i])) << (8 * (i & 3));
+                            x0 = make_uint4(tt[0], tt[1], tt[2], tt[3]);
+                            x1 = make_uint4(tt[4], tt[5], tt[6], tt[7]);
                         }
-                        xdb = __ldg(a.xd + static_cast<int64_t>(m[j]) * nblk + b);
+                        xdb = __ldg(a.xd + static_cast<int64_t>(m[t]) * nblk + b);
                     }
-                    acc[j] = q8_accumulate(acc[j], dot32(w, x0, x1), db, xdb);
+                    acc[t] = q8_accumulate(acc[t], dot32(w[u], x0, x1), d[u], xdb);
                     if (seg_end) {
-                        const float p = warp_sum(acc[j]);
-                        total[j] = seg == 0 ? p : total[j] + p;
-                        acc[j] = 0.0f;
+                        const float p = warp_sum(acc[t]);
+                        tot[t] = seg == 0 ? p : tot[t] + p;
+                        acc[t] = 0.0f;
                     }
                 }
-            }
+                if (s + 1 == nsteps) {
 #pragma unroll
-            for (int j = 0; j < kMoeNT; ++j) {
-                if (m[j] < 0) continue;
-                if (lane == 0) a.y[static_cast<int64_t>(m[j]) * a.Mo + o] = total[j];
+                    for (int t = 0; t < kMoeNT; ++t)
+                        if (m[t] >= 0 && lane == t) a.y[static_cast<int64_t>(m[t]) * a.Mo + cc.o] = tot[t];
+                }
+                if (advance(cc)) {
+                    ++cu;
+                    if (cu < w1) load_tokens();
+                }
             }
         }
+    };
+
+    issue(wA, dA);
+    issue(wB, dB);
+    while (cu < w1) {
+        compute(wA, dA);
+        if (cu >= w1) break;
+        issue(wA, dA);
+        compute(wB, dB);
+        if (cu >= w1) break;
+        issue(wB, dB);
     }
 }
 
@@ -345,7 +448,8 @@ extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E
     if (E > kMoeMaxE || R > kMoeMaxR) return WSW_ERR_UNSUPPORTED;
     if (R == 0 || Mo == 0) return WSW_OK;
     if (!ids || !y || E == 0) return WSW_ERR_INVALID_ARG;
-    if (K > 0 && (!Wq || !Wd || !xq || !xd)) return WSW_ERR_INVALID_ARG;
+    if (K == 0) return WSW_ERR_INVALID_ARG;
+    if (!Wq || !Wd || !xq || !xd) return WSW_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(Wd) & 1) || (reinterpret_cast<uintptr_t>(xd) & 1) ||
         (reinterpret_cast<uintptr_t>(y) & 3) || (reinterpret_cast<uintptr_t>(ids) & 3) ||
         (reinterpret_cast<uintptr_t>(err_flag) & 3))
@@ -357,9 +461,11 @@ extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E
     MoeArgs a;
     a.Wq = Wq; a.Wd = Wd; a.E = E; a.Mo = Mo; a.K = K; a.xq = xq; a.xd = xd; a.ids = ids; a.R = R;
     a.y = y; a.err = err_flag;
-    a.nsteps = (K + Q8::kStepElems - 1) / Q8::kStepElems;
-    a.seg_steps = sg::choose_seg_steps(Mo, static_cast<int>(a.nsteps), di.sm_count);
-    const size_t smem = static_cast<size_t>(4 * E + R) * sizeof(int);
+    a.nsteps = static_cast<int>((K + Q8::kStepElems - 1) / Q8::kStepElems);
+    a.seg_steps = sg::choose_seg_steps(Mo, a.nsteps, di.sm_count);
+    // cnt, off, cur, nbt, ubase[E+1] (int64), used, list
+    const size_t smem = static_cast<size_t>(4 * E) * sizeof(int) + static_cast<size_t>(E + 1) * 8 +
+                        static_cast<size_t>(E + R) * sizeof(int);
     const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 2;
     const unsigned ctas = static_cast<unsigned>(di.sm_count * cps);
     // Weight rows are 16-byte aligned when Wq is and K is a multiple of 16 (it is).
