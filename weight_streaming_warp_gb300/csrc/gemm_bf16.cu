@@ -1,70 +1,370 @@
-// gemm_bf16.cu -- small-batch prefill product Y[n][r] = sum_k W[r][k] * X[n][k].
+// gemm_bf16.cu -- small-batch prefill product Y[n][r] = sum_k W[r][k] * X[n][k] on the
+// fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // Source: "ggml-cuda: pad matmul weight rows to avoid cache-set aliasing" (AMD-Ecosystem
 // llama.cpp PR), Overview and Results: in small-batch prefill a short run of output
-// rows streams the whole weight matrix, the weight's row stride may carry one extra
-// 128-byte line, and the matmul takes its leading dimension from the row stride.
+// rows streams the whole weight matrix; the weight's row stride may carry one extra
+// 128-byte line and the matmul takes its leading dimension from the row stride.
 //
-// Warp-level bf16 tensor-core tiles (m16n8k16, fp32 accumulation): a warp owns 16
-// weight rows and 32 batch columns and walks K in steps of 16; fragments are read
-// straight from global memory (each weight element is fetched by one warp per 32
-// batch columns).
+// Design (GB300):
+//  * A CTA owns a tile of 128 weight rows x NT batch rows (NT a multiple of 16, at most
+//    256; fewer batch rows are zero-filled by the tensor-memory-access engine).  K is
+//    walked in blocks of 64 (128 bytes of bf16 = one 128-byte swizzle row).
+//  * Warp 0 streams W and X blocks with cp.async.bulk.tensor (TMA) into a ring of
+//    shared-memory stages guarded by mbarriers; warp 1 allocates tensor memory and one
+//    of its threads issues tcgen05.mma (M = 128, N = NT, K = 16, bf16 in, fp32
+//    accumulate) and tcgen05.commit to release stages; warps 2-5 are the epilogue,
+//    reading the accumulator with tcgen05.ld (each warp owns its 32 tensor-memory lanes).
+//  * Tiles are few (20 for a 2560-row weight at NT <= 256), so K is split over a
+//    thread-block cluster of S CTAs (S chosen on the host from the cluster occupancy):
+//    each CTA accumulates its share of K, writes the partial tile to its own shared
+//    memory, and after a cluster barrier every rank adds a slice of the tile from all S
+//    ranks through distributed shared memory, ranks first to last.  The reduction order
+//    is fixed, so results are deterministic and do not depend on the row stride.
+//  * Every mbarrier wait is bounded; a wait that runs out marks the tile with NaN and
+//    the CTA still reaches its tensor-memory release.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "common.cuh"
 
 namespace wsw {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kNB = 4;  // 8-column MMA tiles per warp
+constexpr int kBM = 128;            // weight rows per tile (MMA M)
+constexpr int kBK = 64;             // K elements per stage
+constexpr int kThreadsG = 192;      // warp 0: TMA, warp 1: TMEM + MMA, warps 2-5: epilogue
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB per stage
 
-__device__ __forceinline__ uint32_t ld_pair(const uint16_t *base, int64_t row, int64_t nrows,
-                                            int64_t ld, int64_t k, int64_t K) {
-    if (row >= nrows) return 0u;
-    const uint16_t *p = base + row * ld + k;
-    if (k + 1 < K) return *reinterpret_cast<const uint32_t *>(p);
-    if (k < K) return static_cast<uint32_t>(p[0]);
-    return 0u;
+struct GemmArgs {
+    int64_t M, N, K;
+    float *Y;
+    int nt;       // batch rows per tile
+    int n_tiles;  // ceil(N / nt)
+    int kblocks;  // ceil(K / 64)
+    int stages;
+};
+
+__device__ __forceinline__ uint32_t saddr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__global__ void __launch_bounds__(kWarps * 32) gemm_bf16_mma_kernel(
-    const uint16_t *__restrict__ W, int64_t M, int64_t K, int64_t ld, const uint16_t *__restrict__ X,
-    int64_t N, int64_t ldx, float *__restrict__ Y) {
-    pdl_launch_dependents();
-    pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int g = lane >> 2, tg = lane & 3;
-    const int64_t r0 = (static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * 16;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.y) * 8 * kNB;
-    if (r0 >= M) return;
-    float c[kNB][4];
-#pragma unroll
-    for (int j = 0; j < kNB; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
-    for (int64_t k0 = 0; k0 < K; k0 += 16) {
-        const uint32_t a0 = ld_pair(W, r0 + g, M, ld, k0 + 2 * tg, K);
-        const uint32_t a1 = ld_pair(W, r0 + g + 8, M, ld, k0 + 2 * tg, K);
-        const uint32_t a2 = ld_pair(W, r0 + g, M, ld, k0 + 2 * tg + 8, K);
-        const uint32_t a3 = ld_pair(W, r0 + g + 8, M, ld, k0 + 2 * tg + 8, K);
-#pragma unroll
-        for (int j = 0; j < kNB; ++j) {
-            const int64_t n = n0 + 8 * j + g;
-            const uint32_t b0 = ld_pair(X, n, N, ldx, k0 + 2 * tg, K);
-            const uint32_t b1 = ld_pair(X, n, N, ldx, k0 + 2 * tg + 8, K);
-            asm volatile(
-                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-                : "+f"(c[j][0]), "+f"(c[j][1]), "+f"(c[j][2]), "+f"(c[j][3])
-                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete; give up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(saddr(b)), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((i & 1023u) == 0) {
+            const uint64_t t = global_ns();
+            if (i == 0) t0 = t;
+            else if (t - t0 > kWaitLimitNs) return false;
         }
     }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(saddr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);  // start address
+    d |= static_cast<uint64_t>(1) << 16;                 // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;         // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                 // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                 // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t instr_desc(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dtmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int j = 0; j < kNB; ++j) {
-        const int64_t n = n0 + 8 * j + 2 * tg;
-        const int64_t r = r0 + g;
-        if (n < N && r < M) Y[n * M + r] = c[j][0];
-        if (n + 1 < N && r < M) Y[(n + 1) * M + r] = c[j][1];
-        if (n < N && r + 8 < M) Y[n * M + r + 8] = c[j][2];
-        if (n + 1 < N && r + 8 < M) Y[(n + 1) * M + r + 8] = c[j][3];
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_dsmem(const float *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(kThreadsG, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                        const GemmArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int stages = a.stages;
+    const int nt = a.nt;
+    const uint32_t b_bytes = static_cast<uint32_t>(nt) * kBK * 2;
+    unsigned char *sA = smem;
+    unsigned char *sB = smem + static_cast<size_t>(stages) * kABytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + static_cast<size_t>(stages) * b_bytes);
+    uint64_t *empty = full + stages;
+    uint64_t *accum = empty + stages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+    float *part = reinterpret_cast<float *>(smem);  // reuses the stages after the main loop
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t S = cluster_size();
+    const uint32_t rank = cluster_rank();
+    const int64_t tile = blockIdx.x / S;
+    const int64_t m_tile = tile / a.n_tiles;
+    const int n_tile = static_cast<int>(tile % a.n_tiles);
+    const int64_t m0 = m_tile * kBM;
+    const int n0 = n_tile * nt;
+    const int kb0 = static_cast<int>(static_cast<int64_t>(rank) * a.kblocks / S);
+    const int kb1 = static_cast<int>(static_cast<int64_t>(rank + 1) * a.kblocks / S);
+    const int nk = kb1 - kb0;
+    const uint32_t tcols = nt <= 32 ? 32 : (nt <= 64 ? 64 : (nt <= 128 ? 128 : 256));
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accum, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                     "r"(tcols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint64_t pol_w, pol_x;
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
+            pdl_wait();  // X is written by earlier kernels
+            for (int i = 0; i < nk && ok; ++i) {
+                const int s = i % stages;
+                const uint32_t round = static_cast<uint32_t>(i / stages);
+                if (!mbar_wait(&empty[s], (round & 1u) ^ 1u)) { ok = false; break; }
+                mbar_expect_tx(&full[s], kABytes + b_bytes);
+                const int k = (kb0 + i) * kBK;
+                tma_load_2d(sA + static_cast<size_t>(s) * kABytes, &tmW, k, static_cast<int>(m0), &full[s], pol_w);
+                tma_load_2d(sB + static_cast<size_t>(s) * b_bytes, &tmX, k, n0, &full[s], pol_x);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc(kBM, nt);
+            for (int i = 0; i < nk && ok; ++i) {
+                const int s = i % stages;
+                const uint32_t round = static_cast<uint32_t>(i / stages);
+                if (!mbar_wait(&full[s], round & 1u)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t da = sw128_desc(saddr(sA + static_cast<size_t>(s) * kABytes));
+                const uint64_t db = sw128_desc(saddr(sB + static_cast<size_t>(s) * b_bytes));
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per MMA: +32 bytes per step
+                    mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (i | kk) != 0);
+                mma_commit(&empty[s]);
+            }
+            mma_commit(accum);
+        }
+        __syncwarp();
+    } else {
+        // epilogue: warp w owns tensor-memory lanes 32*(w % 4) .. +31 = tile rows
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const int64_t m = m0 + row;
+        const bool have = mbar_wait(accum, 0);
+        tc_fence_after();
+        for (int c = 0; c < nt; c += 16) {
+            float v[16];
+            if (have) {
+                tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c), v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = __int_as_float(0x7fc00000);
+            }
+            if (S == 1) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int64_t n = n0 + c + j;
+                    if (n < a.N && m < a.M) a.Y[n * a.M + m] = v[j];
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) part[(c + j) * kBM + row] = v[j];
+            }
+        }
+    }
+
+    if (S > 1) {
+        // Split-K: every rank adds a slice of the tile from all ranks, in rank order.
+        cluster_sync();
+        const int elems = nt * kBM;
+        const int e0 = static_cast<int>(static_cast<int64_t>(rank) * elems / S);
+        const int e1 = static_cast<int>(static_cast<int64_t>(rank + 1) * elems / S);
+        for (int e = e0 + threadIdx.x; e < e1; e += kThreadsG) {
+            float sum = ld_dsmem(part + e, 0);
+            for (uint32_t r = 1; r < S; ++r) sum += ld_dsmem(part + e, r);
+            const int64_t n = n0 + e / kBM;
+            const int64_t m = m0 + e % kBM;
+            if (n < a.N && m < a.M) a.Y[n * a.M + m] = sum;
+        }
+        cluster_sync();  // peers keep their shared memory until every rank has read it
+    }
+    pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tcols) : "memory");
+    }
+}
+
+// --------------------------------------------------------------------- host --
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map: `rows` rows of `cols` elements, row pitch `ld` elements, box
+// of 64 x box_rows with 128-byte swizzle; out-of-range elements read as zero.
+bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t smem_bytes(int stages, int nt) {
+    return 1024 + static_cast<size_t>(stages) * (kABytes + static_cast<size_t>(nt) * kBK * 2) +
+           static_cast<size_t>(2 * stages + 1) * 8 + 16;
+}
+
+// Clusters of `s` CTAs that fit on the device at once (cached per size and smem).
+int max_clusters(int s, size_t smem) {
+    static std::map<std::pair<int, size_t>, int> cache;
+    static std::mutex mu;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(s * 64 + dev, smem);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s) * 32);
+    cfg.blockDim = dim3(kThreadsG);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(s);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(gemm_bf16_tc_kernel), &cfg) != cudaSuccess)
+        n = 0;
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = n;
+    return n;
 }
 
 }  // namespace
@@ -82,14 +382,64 @@ extern "C" int wsw_gemm_bf16(const uint16_t *W, int64_t M, int64_t K, int64_t ld
     if ((reinterpret_cast<uintptr_t>(W) & 15) || (reinterpret_cast<uintptr_t>(X) & 15) ||
         (reinterpret_cast<uintptr_t>(Y) & 3) || (K % 8) || (ld % 8) || (ldx % 8))
         return WSW_ERR_MISALIGNED;
-    if (M > (int64_t(1) << 31) || N > 65535 * 8 * kNB) return WSW_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31) || K > (int64_t(1) << 31)) return WSW_ERR_INVALID_ARG;
     DeviceInfo di;
     if (!device_info(&di, &st)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0)
         return cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * 4, s) == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
-    const dim3 grid(static_cast<unsigned>((M + 16 * kWarps - 1) / (16 * kWarps)),
-                    static_cast<unsigned>((N + 8 * kNB - 1) / (8 * kNB)));
-    cudaError_t e = launch(gemm_bf16_mma_kernel, grid, dim3(kWarps * 32), 0, s, o.pdl, W, M, K, ld, X, N, ldx, Y);
+
+    GemmArgs a;
+    a.M = M; a.N = N; a.K = K; a.Y = Y;
+    a.n_tiles = static_cast<int>((N + 255) / 256);
+    a.nt = static_cast<int>(((N + a.n_tiles - 1) / a.n_tiles + 15) / 16 * 16);
+    a.kblocks = static_cast<int>((K + kBK - 1) / kBK);
+    const int b_bytes = a.nt * kBK * 2;
+    a.stages = (kSmemBudget - 2048) / (kABytes + b_bytes);
+    if (a.stages > 8) a.stages = 8;
+    if (a.stages < 2) return WSW_ERR_UNSUPPORTED;
+    // the partial tile of a split must fit in the stage buffers
+    if (static_cast<size_t>(a.nt) * kBM * 4 > static_cast<size_t>(a.stages) * (kABytes + b_bytes))
+        return WSW_ERR_UNSUPPORTED;
+    const size_t smem = smem_bytes(a.stages, a.nt);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * a.n_tiles;
+    if (tiles * 8 > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
+
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(gemm_bf16_tc_kernel), static_cast<int>(smem));
+    if (e != cudaSuccess) return WSW_ERR_CUDA;
+
+    // Split-K cluster size: the fewest waves x K-blocks per CTA (ties: smaller S).
+    int best_s = 1;
+    int64_t best_cost = -1;
+    for (int sp = 1; sp <= 8 && sp <= a.kblocks; ++sp) {
+        const int cap = max_clusters(sp, smem);
+        if (cap <= 0) continue;
+        const int64_t waves = (tiles + cap - 1) / cap;
+        const int64_t cost = waves * ((a.kblocks + sp - 1) / sp) + (sp > 1 ? 2 : 0);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_s = sp; }
+    }
+
+    CUtensorMap tmW, tmX;
+    if (!make_map(&tmW, W, M, K, ld, kBM) || !make_map(&tmX, X, N, K, ldx, a.nt)) return WSW_ERR_CUDA;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * best_s));
+    cfg.blockDim = dim3(kThreadsG);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(best_s);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int nattr = 1;
+    if (o.pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        nattr = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    e = cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel, tmW, tmX, a);
     return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
 }
