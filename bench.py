@@ -236,16 +236,24 @@ def _time_graph(torch, g, reps):
     return e0.elapsed_time(e1) / 1000.0 / reps
 
 
-def _traffic_record(kernel_file):
-    """DRAM traffic per launch from the committed ncu summary, or None when the
-    kernel's source changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {"gemv_q8_0": ("gemv_q8_0.cu", "stream_gemv.cuh", "common.cuh")}
+
+
+def kernel_source_sha(name):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[name]:
+        with open(os.path.join(ROOT, "weight_streaming_warp_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _traffic_record(name):
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json),
+    or None when the kernel's sources changed since the counters were taken."""
     try:
-        with open(path) as f:
-            rec = json.load(f)
-        src = open(os.path.join(ROOT, "weight_streaming_warp_gb300", "csrc", kernel_file), "rb").read()
-        r = rec.get(kernel_file)
-        if r and r.get("source_sha256") == hashlib.sha256(src).hexdigest():
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            r = json.load(f).get(name)
+        if r and r.get("source_sha256") == kernel_source_sha(name):
             return r["bytes_per_launch"]
     except Exception:
         pass
@@ -560,7 +568,7 @@ def run_ours(args):
         "roofline": {"kernel": "gemv_q8_0_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": _traffic_record("gemv_q8_0.cu"),
+                     "traffic": _traffic_record("gemv_q8_0"),
                      "algorithmic_bytes_per_launch": B_GEMV,
                      "launch_us": {"median": round(k_med * 1e6, 3), "min": round(k_min * 1e6, 3),
                                    "max": round(k_max * 1e6, 3)}},

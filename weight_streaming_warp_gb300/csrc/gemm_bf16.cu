@@ -9,7 +9,9 @@
 // Design (GB300):
 //  * A CTA owns a tile of 128 weight rows x NT batch rows (NT a multiple of 16, at most
 //    256; fewer batch rows are zero-filled by the tensor-memory-access engine).  K is
-//    walked in blocks of 64 (128 bytes of bf16 = one 128-byte swizzle row).
+//    walked in stages of one or two 64-element boxes (128 bytes of bf16 = one 128-byte
+//    swizzle row per box); the memory-bound small-NT tiles take two, so that 256
+//    consecutive bytes of each weight row are requested together.
 //  * Warp 0 streams W and X blocks with cp.async.bulk.tensor (TMA) into a ring of
 //    shared-memory stages guarded by mbarriers; warp 1 allocates tensor memory and one
 //    of its threads issues tcgen05.mma (M = 128, N = NT, K = 16, bf16 in, fp32
@@ -36,18 +38,20 @@ namespace wsw {
 namespace {
 
 constexpr int kBM = 128;            // weight rows per tile (MMA M)
-constexpr int kBK = 64;             // K elements per stage
+constexpr int kAtom = 64;           // K elements per 128-byte swizzle atom (one TMA box)
 constexpr int kThreadsG = 192;      // warp 0: TMA, warp 1: TMEM + MMA, warps 2-5: epilogue
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr int kSmemBudget = 200 * 1024;
-constexpr int kABytes = kBM * kBK * 2;  // 16 KB per stage
+constexpr int kAtomA = kBM * kAtom * 2;  // 16 KB: one weight box
+constexpr int kMaxSplit = 8;            // cluster size limit (portable)
 
 struct GemmArgs {
     int64_t M, N, K;
     float *Y;
     int nt;       // batch rows per tile
     int n_tiles;  // ceil(N / nt)
-    int kblocks;  // ceil(K / 64)
+    int atoms;    // 64-element boxes per stage (1 or 2)
+    int kblocks;  // ceil(K / (64 * atoms))
     int stages;
 };
 
@@ -68,9 +72,10 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Wait for the phase with the given parity to complete; give up after kWaitLimitNs.
+// The clock is read only once a wait has already spun for a while.
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
     uint64_t t0 = 0;
-    for (uint32_t i = 0;; ++i) {
+    for (uint32_t i = 1;; ++i) {
         uint32_t done;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
@@ -80,7 +85,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
         if (done) return true;
         if ((i & 1023u) == 0) {
             const uint64_t t = global_ns();
-            if (i == 0) t0 = t;
+            if (t0 == 0) t0 = t;
             else if (t - t0 > kWaitLimitNs) return false;
         }
     }
@@ -155,11 +160,16 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float ld_dsmem(const float *local, uint32_t rank) {
+// 16 bytes of a cluster peer's shared memory at the same offset as `local`.  Issued
+// without a memory clobber so that several of them can be in flight at once (the
+// cluster barrier before the reads orders them after the peers' writes).
+__device__ __forceinline__ float4 ld_dsmem4(const float *local, uint32_t rank) {
     uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr(local)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote));
     return v;
 }
 
@@ -171,9 +181,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int stages = a.stages;
     const int nt = a.nt;
-    const uint32_t b_bytes = static_cast<uint32_t>(nt) * kBK * 2;
+    const int atoms = a.atoms;
+    const uint32_t a_bytes = static_cast<uint32_t>(atoms) * kAtomA;
+    const uint32_t b_bytes = static_cast<uint32_t>(atoms) * nt * kAtom * 2;
     unsigned char *sA = smem;
-    unsigned char *sB = smem + static_cast<size_t>(stages) * kABytes;
+    unsigned char *sB = smem + static_cast<size_t>(stages) * a_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(sB + static_cast<size_t>(stages) * b_bytes);
     uint64_t *empty = full + stages;
     uint64_t *accum = empty + stages;
@@ -219,15 +231,22 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             uint64_t pol_w, pol_x;
             asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
             asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
             pdl_wait();  // X is written by earlier kernels
             for (int i = 0; i < nk && ok; ++i) {
                 const int s = i % stages;
                 const uint32_t round = static_cast<uint32_t>(i / stages);
                 if (!mbar_wait(&empty[s], (round & 1u) ^ 1u)) { ok = false; break; }
-                mbar_expect_tx(&full[s], kABytes + b_bytes);
-                const int k = (kb0 + i) * kBK;
-                tma_load_2d(sA + static_cast<size_t>(s) * kABytes, &tmW, k, static_cast<int>(m0), &full[s], pol_w);
-                tma_load_2d(sB + static_cast<size_t>(s) * b_bytes, &tmX, k, n0, &full[s], pol_x);
+                mbar_expect_tx(&full[s], a_bytes + b_bytes);
+                const int k = (kb0 + i) * kAtom * atoms;
+                // consecutive 128-byte pieces of each weight row are requested back to back
+                for (int j = 0; j < atoms; ++j)
+                    tma_load_2d(sA + static_cast<size_t>(s) * a_bytes + j * kAtomA, &tmW, k + j * kAtom,
+                                static_cast<int>(m0), &full[s], pol_w);
+                for (int j = 0; j < atoms; ++j)
+                    tma_load_2d(sB + static_cast<size_t>(s) * b_bytes + j * (nt * kAtom * 2), &tmX, k + j * kAtom, n0,
+                                &full[s], pol_x);
             }
         }
         __syncwarp();
@@ -239,11 +258,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                 const uint32_t round = static_cast<uint32_t>(i / stages);
                 if (!mbar_wait(&full[s], round & 1u)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t da = sw128_desc(saddr(sA + static_cast<size_t>(s) * kABytes));
-                const uint64_t db = sw128_desc(saddr(sB + static_cast<size_t>(s) * b_bytes));
+                for (int j = 0; j < atoms; ++j) {
+                    const uint64_t da = sw128_desc(saddr(sA + static_cast<size_t>(s) * a_bytes + j * kAtomA));
+                    const uint64_t db = sw128_desc(saddr(sB + static_cast<size_t>(s) * b_bytes + j * (nt * kAtom * 2)));
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)  // K = 16 per MMA: +32 bytes per step
-                    mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (i | kk) != 0);
+                    for (int kk = 0; kk < kAtom / 16; ++kk)  // K = 16 per MMA: +32 bytes within the atom
+                        mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (i | j | kk) != 0);
+                }
                 mma_commit(&empty[s]);
             }
             mma_commit(accum);
@@ -280,15 +301,38 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     if (S > 1) {
         // Split-K: every rank adds a slice of the tile from all ranks, in rank order.
         cluster_sync();
-        const int elems = nt * kBM;
-        const int e0 = static_cast<int>(static_cast<int64_t>(rank) * elems / S);
-        const int e1 = static_cast<int>(static_cast<int64_t>(rank + 1) * elems / S);
-        for (int e = e0 + threadIdx.x; e < e1; e += kThreadsG) {
-            float sum = ld_dsmem(part + e, 0);
-            for (uint32_t r = 1; r < S; ++r) sum += ld_dsmem(part + e, r);
-            const int64_t n = n0 + e / kBM;
-            const int64_t m = m0 + e % kBM;
-            if (n < a.N && m < a.M) a.Y[n * a.M + m] = sum;
+        const int quads = nt * kBM / 4;  // 4 consecutive tile rows of one batch row
+        const int q0 = static_cast<int>(static_cast<int64_t>(rank) * quads / S);
+        const int q1 = static_cast<int>(static_cast<int64_t>(rank + 1) * quads / S);
+        const bool vec_store = (a.M % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.Y) & 15) == 0);
+        for (int qd = q0 + threadIdx.x; qd < q1; qd += kThreadsG) {
+            float4 v[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                if (r < static_cast<int>(S)) v[r] = ld_dsmem4(part + 4 * qd, static_cast<uint32_t>(r));
+            float4 sum = v[0];
+#pragma unroll
+            for (int r = 1; r < 8; ++r) {
+                if (r < static_cast<int>(S)) {
+                    sum.x += v[r].x;
+                    sum.y += v[r].y;
+                    sum.z += v[r].z;
+                    sum.w += v[r].w;
+                }
+            }
+            const int64_t n = n0 + (4 * qd) / kBM;
+            const int64_t m = m0 + (4 * qd) % kBM;
+            if (n < a.N) {
+                float *dst = a.Y + n * a.M + m;
+                if (vec_store && m + 3 < a.M) {
+                    *reinterpret_cast<float4 *>(dst) = sum;
+                } else {
+                    const float t[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (m + i < a.M) dst[i] = t[i];
+                }
+            }
         }
         cluster_sync();  // peers keep their shared memory until every rank has read it
     }
@@ -324,15 +368,15 @@ bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, in
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kAtom), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t smem_bytes(int stages, int nt) {
-    return 1024 + static_cast<size_t>(stages) * (kABytes + static_cast<size_t>(nt) * kBK * 2) +
+size_t smem_bytes(int stages, int nt, int atoms) {
+    return 1024 + static_cast<size_t>(stages) * atoms * (kAtomA + static_cast<size_t>(nt) * kAtom * 2) +
            static_cast<size_t>(2 * stages + 1) * 8 + 16;
 }
 
@@ -393,15 +437,17 @@ extern "C" int wsw_gemm_bf16(const uint16_t *W, int64_t M, int64_t K, int64_t ld
     a.M = M; a.N = N; a.K = K; a.Y = Y;
     a.n_tiles = static_cast<int>((N + 255) / 256);
     a.nt = static_cast<int>(((N + a.n_tiles - 1) / a.n_tiles + 15) / 16 * 16);
-    a.kblocks = static_cast<int>((K + kBK - 1) / kBK);
-    const int b_bytes = a.nt * kBK * 2;
-    a.stages = (kSmemBudget - 2048) / (kABytes + b_bytes);
+    // Memory-bound tiles (few batch rows) read 256 bytes of each weight row per stage;
+    // compute-bound ones keep 128-byte stages and more of them.
+    a.atoms = a.nt <= 128 ? 2 : 1;
+    a.kblocks = static_cast<int>((K + kAtom * a.atoms - 1) / (kAtom * a.atoms));
+    const int stage_bytes = a.atoms * (kAtomA + a.nt * kAtom * 2);
+    a.stages = (kSmemBudget - 2048) / stage_bytes;
     if (a.stages > 8) a.stages = 8;
     if (a.stages < 2) return WSW_ERR_UNSUPPORTED;
     // the partial tile of a split must fit in the stage buffers
-    if (static_cast<size_t>(a.nt) * kBM * 4 > static_cast<size_t>(a.stages) * (kABytes + b_bytes))
-        return WSW_ERR_UNSUPPORTED;
-    const size_t smem = smem_bytes(a.stages, a.nt);
+    if (static_cast<size_t>(a.nt) * kBM * 4 > static_cast<size_t>(a.stages) * stage_bytes) return WSW_ERR_UNSUPPORTED;
+    const size_t smem = smem_bytes(a.stages, a.nt, a.atoms);
     const int64_t tiles = ((M + kBM - 1) / kBM) * a.n_tiles;
     if (tiles * 8 > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
 
@@ -411,7 +457,7 @@ extern "C" int wsw_gemm_bf16(const uint16_t *W, int64_t M, int64_t K, int64_t ld
     // Split-K cluster size: the fewest waves x K-blocks per CTA (ties: smaller S).
     int best_s = 1;
     int64_t best_cost = -1;
-    for (int sp = 1; sp <= 8 && sp <= a.kblocks; ++sp) {
+    for (int sp = 1; sp <= kMaxSplit && sp <= a.kblocks; ++sp) {
         const int cap = max_clusters(sp, smem);
         if (cap <= 0) continue;
         const int64_t waves = (tiles + cap - 1) / cap;
