@@ -120,10 +120,10 @@ def test_empty_and_single_row():
 
 
 def test_every_output_written_and_equal_to_dense(orc):
-    """Experts with many rows (several token batches): every y entry is written, and
-    sampled rows equal the dense mat-vec on their expert bit for bit."""
+    """Experts with several token batches (CUDA-core form, <= 256 rows): every y entry
+    is written, and sampled rows equal the dense mat-vec on their expert bit for bit."""
     wsw = need_gpu()
-    En, Mo, K, T = 16, 256, 512, 128
+    En, Mo, K, T = 8, 256, 512, 32
     g = np.random.default_rng(11)
     Wq = g.integers(-127, 128, size=(En, Mo, K)).astype(np.int8)
     Wd = g.integers(0x0800, 0x1c00, size=(En, Mo, K // 32)).astype(np.uint16)
@@ -140,3 +140,35 @@ def test_every_output_written_and_equal_to_dense(orc):
         e = ids[m]
         yd = wsw.gemv_q8_0(Wqd[e], Wdd[e], torch.from_numpy(xq[m]).cuda(), u16_to_torch(xd[m], torch.float16).cuda())
         assert torch.equal(yd.view(torch.int32), y[m].view(torch.int32)), m
+
+
+@pytest.mark.parametrize("Mo,K,T,En,topk", [(200, 256, 200, 4, 2), (128, 768, 64, 16, 8), (384, 2048, 48, 8, 8)])
+def test_tensor_core_form_against_oracle(orc, Mo, K, T, En, topk):
+    """More than 256 rows: exact integer block sums on the tensor cores.  Experts with
+    more than 64 rows (several token tiles), a partial 128-row tile, every output
+    written and within 1e-4 of the fp64 oracle; a bad id is flagged and skipped."""
+    wsw = need_gpu()
+    g = np.random.default_rng(Mo + K + T)
+    W = syn.normal(4, "tc%d_%d" % (Mo, K), (En * Mo, K), 0.02, torch.bfloat16).float().numpy()
+    Wq, Wd = orc.quantize_q8(W, 32)
+    Wq, Wd = Wq.reshape(En, Mo, K), Wd.reshape(En, Mo, K // 32)
+    ids = syn.routing(4, "tc_route", T, En, topk).numpy()
+    R = T * topk
+    ids[5] = En  # out of range
+    x = syn.normal(4, "tc_x%d" % K, (R, K)).numpy()
+    xq, xd = orc.quantize_q8(x, 32)
+    y = torch.full((R, Mo), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wsw.moe_gemv_q8_0(torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda(),
+                      torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda(),
+                      torch.from_numpy(ids).cuda(), out=y, err_flag=err)
+    yc = y.cpu().numpy()
+    assert err.item() != 0
+    assert np.isnan(yc[5]).all()
+    y64, bad = orc.moe_gemv_q8_0(Wq, Wd, xq, xd, ids)
+    assert bad == 1
+    for m in range(R):
+        if m == 5:
+            continue
+        e = ids[m]
+        check_tol(yc[m], y64[m], mag_q8(Wq[e], Wd[e], xq[m], xd[m]), TOL_Q8, "row %d" % m)

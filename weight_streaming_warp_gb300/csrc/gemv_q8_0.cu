@@ -19,6 +19,7 @@
 // work decomposition is in stream_gemv.cuh).
 #include <cuda_fp16.h>
 
+#include "moe_tc.cuh"
 #include "stream_gemv.cuh"
 
 namespace wsw {
@@ -160,6 +161,7 @@ constexpr int kMoeNT = 4;         // rows of one expert per pass over a weight r
 constexpr int kMoeU = 4;          // steps per register batch
 constexpr int kMoeMaxE = 1024;
 constexpr int kMoeMaxR = 16384;
+constexpr int64_t kMoeTcMinRows = 256;  // more rows than this: tensor-core form
 
 struct MoeArgs {
     const int8_t *Wq;
@@ -173,6 +175,8 @@ struct MoeArgs {
     int32_t *err;
     int nsteps;     // ceil(K / 1024)
     int seg_steps;  // as the dense kernel on one expert's Mo x K matrix
+    int xs_cap;     // activation rows that fit the shared-memory staging area
+    int64_t xs_off; // byte offset of that area in dynamic shared memory
 };
 
 // Shared memory: cnt[E], off[E], cur[E], nbt[E] (token batches), ubase[E+1] (first
@@ -263,17 +267,50 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gemv_q8_0_kernel(const MoeArg
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
     const int64_t warp = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
     const int64_t w0 = warp * total / nwarps, w1 = (warp + 1) * total / nwarps;
-    if (w0 >= w1) return;
     const int nsteps = a.nsteps;
     const int64_t nblk = a.K / 32;
     const uint64_t pol = policy_evict_first();
 
-    // locate the first unit: used expert index by binary search over ubase
-    int lo = 0, hi = nused - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (ubase[mid] <= w0) lo = mid; else hi = mid - 1;
+    // used-expert index of a unit (binary search over ubase)
+    auto find_unit = [&](int64_t u) {
+        int lo = 0, hi = nused - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ubase[mid] <= u) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+    };
+
+    // Stage the activation rows of the experts this CTA's units cover (a contiguous
+    // range of the row lists) in shared memory, when they fit: two planes of 16-byte
+    // halves [2][ntok][nblk] and the scales [ntok][nblk].
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kWarps * total / nwarps;
+    const int64_t c1 = static_cast<int64_t>(blockIdx.x + 1) * kWarps * total / nwarps;
+    int tl0 = 0, ntok = 0;
+    if (c0 < c1) {
+        const int ea = used[find_unit(c0)], eb = used[find_unit(c1 - 1)];
+        tl0 = off[ea];
+        ntok = off[eb] + cnt[eb] - tl0;
     }
+    const bool staged = ntok > 0 && ntok <= a.xs_cap && (reinterpret_cast<uintptr_t>(a.xq) & 15) == 0;
+    uint4 *xs = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(moe_smem) + a.xs_off);
+    uint16_t *xsd = reinterpret_cast<uint16_t *>(xs + 2 * static_cast<int64_t>(ntok) * nblk);
+    if (staged) {
+        for (int64_t h = threadIdx.x; h < 2 * ntok * nblk; h += kThreads) {
+            const int64_t slot = h / (2 * nblk), rem = h - slot * 2 * nblk;  // rem = 2 * block + half
+            const int64_t m = list[tl0 + slot];
+            xs[((rem & 1) * ntok + slot) * nblk + (rem >> 1)] =
+                __ldg(reinterpret_cast<const uint4 *>(a.xq + m * a.K) + rem);
+        }
+        for (int64_t h = threadIdx.x; h < ntok * nblk; h += kThreads) {
+            const int64_t slot = h / nblk, b = h - slot * nblk;
+            xsd[h] = a.xd[static_cast<int64_t>(list[tl0 + slot]) * nblk + b];
+        }
+    }
+    __syncthreads();
+    if (w0 >= w1) return;
+
+    const int lo = find_unit(w0);
     struct Cursor {
         int ui;      // used-expert index
         int e, nb;   // expert, its token batches
@@ -325,10 +362,12 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gemv_q8_0_kernel(const MoeArg
     };
 
     int m[kMoeNT];
+    int slot0 = 0;  // staging slot of the unit's first row (rows of a batch are consecutive)
     float acc[kMoeNT], tot[kMoeNT];
     auto load_tokens = [&]() {
         const int base = off[cc.e] + cc.j * kMoeNT;
         const int left = cnt[cc.e] - cc.j * kMoeNT;
+        slot0 = base - tl0;
 #pragma unroll
         for (int t = 0; t < kMoeNT; ++t) {
             m[t] = t < left ? list[base + t] : -1;
@@ -351,7 +390,12 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gemv_q8_0_kernel(const MoeArg
                     if (m[t] < 0) continue;  // warp-uniform
                     uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
                     uint32_t xdb = 0u;
-                    if (valid) {
+                    if (valid && staged) {
+                        const int64_t sl = slot0 + t;
+                        x0 = xs[sl * nblk + b];
+                        x1 = xs[(ntok + sl) * nblk + b];
+                        xdb = xsd[sl * nblk + b];
+                    } else if (valid) {
                         const int8_t *xr = a.xq + static_cast<int64_t>(m[t]) * a.K + 32 * b;
                         if ((reinterpret_cast<uintptr_t>(xr) & 15) == 0) {
                             x0 = __ldg(reinterpret_cast<const uint4 *>(xr));
@@ -458,14 +502,25 @@ extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E
     DeviceInfo di;
     if (!device_info(&di, &st)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (R > kMoeTcMinRows && moe_q8_tc_supported(E, Mo, K, R, Wq, Wd, xq, xd)) {
+        MoeTcArgs t;
+        t.Wq = Wq; t.Wd = Wd; t.E = E; t.Mo = Mo; t.K = K; t.xq = xq; t.xd = xd; t.ids = ids; t.R = R;
+        t.y = y; t.err = err_flag;
+        return moe_q8_tc_launch(t, s, o.pdl);
+    }
     MoeArgs a;
     a.Wq = Wq; a.Wd = Wd; a.E = E; a.Mo = Mo; a.K = K; a.xq = xq; a.xd = xd; a.ids = ids; a.R = R;
     a.y = y; a.err = err_flag;
     a.nsteps = static_cast<int>((K + Q8::kStepElems - 1) / Q8::kStepElems);
     a.seg_steps = sg::choose_seg_steps(Mo, a.nsteps, di.sm_count);
-    // cnt, off, cur, nbt, ubase[E+1] (int64), used, list
-    const size_t smem = static_cast<size_t>(4 * E) * sizeof(int) + static_cast<size_t>(E + 1) * 8 +
-                        static_cast<size_t>(E + R) * sizeof(int);
+    // cnt, off, cur, nbt, ubase[E+1] (int64), used, list, then the activation staging area
+    const size_t base_smem = (static_cast<size_t>(4 * E) * sizeof(int) + static_cast<size_t>(E + 1) * 8 +
+                              static_cast<size_t>(E + R) * sizeof(int) + 15) & ~static_cast<size_t>(15);
+    const size_t per_row = static_cast<size_t>(K) + static_cast<size_t>(K / 32) * 2;  // int8 + scales
+    const size_t x_budget = 64 * 1024;
+    a.xs_cap = static_cast<int>(x_budget / per_row);
+    a.xs_off = static_cast<int64_t>(base_smem);
+    const size_t smem = base_smem + static_cast<size_t>(a.xs_cap) * per_row;
     const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 2;
     const unsigned ctas = static_cast<unsigned>(di.sm_count * cps);
     // Weight rows are 16-byte aligned when Wq is and K is a multiple of 16 (it is).
