@@ -19,9 +19,8 @@
 //    16c + 4q .. 16c + 4q + 3 of chunk c in plane q), so per-lane reads are
 //    conflict-free; for K > 25600 x is read through L1 instead.
 //  * Weights use L1::no_allocate + L2 evict_first loads, double-buffered in registers.
-//  * With PDL, each warp issues its first batch of weight loads and an L2 prefetch of
-//    the start of its stream before griddepcontrol.wait, i.e. while the previous
-//    mat-vec drains.
+//  * With PDL, each warp issues both register batches of weight loads before
+//    griddepcontrol.wait, i.e. while the previous mat-vec drains.
 #include "stream_gemv.cuh"
 
 namespace wsw {
@@ -30,6 +29,7 @@ namespace {
 constexpr int kMaxSmemSteps = 50;  // x staged in shared memory up to K = 25600
 
 struct Bf16 {
+    static constexpr int kWarps = 16;  // warps per CTA
     static constexpr int kStepElems = 512;
     static constexpr bool kGlobalX = true;  // x may be read through L1 instead of staged
     struct Args {
@@ -40,6 +40,10 @@ struct Bf16 {
         float alpha;
         float *y;
     };
+    __device__ __forceinline__ static const char *row_ptr(const Args &a, int64_t row) {
+        return reinterpret_cast<const char *>(a.W + row * a.ld);
+    }
+    __device__ __forceinline__ static int64_t row_bytes(const Args &a) { return a.K * 2; }
     struct Buf { uint32_t w[8]; };
     struct Acc { float a0, a1; };
     struct XVal { float4 q[4]; };
@@ -69,19 +73,13 @@ struct Bf16 {
 #pragma unroll
         for (int i = 0; i < 8; ++i) b.w[i] = 0u;
     }
-    __device__ __forceinline__ static void prefetch(const Args &a, int64_t row, int step, int lane) {
-        const char *p = reinterpret_cast<const char *>(a.W + row * a.ld);
-        const int64_t end = 2 * a.K;
-        int64_t begin = static_cast<int64_t>(step) * 1024 + 4096;  // past the first batch
-        for (int64_t off = begin + lane * 128; off < end && off < begin + 8192; off += 32 * 128) prefetch_l2(p + off);
-    }
     template <bool XS>
     __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
         if constexpr (XS) {
             float4 *xs = reinterpret_cast<float4 *>(xsm);
             const int64_t nchunks = static_cast<int64_t>(nsteps) * 32;
             const bool xvec = (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
-            for (int64_t q = threadIdx.x; q < 4 * nchunks; q += sg::kThreads) {
+            for (int64_t q = threadIdx.x; q < 4 * nchunks; q += blockDim.x) {
                 // quad q = elements 4q .. 4q+3 = plane (q & 3) of chunk q >> 2
                 const int64_t e0 = 4 * q;
                 float4 v;
@@ -162,11 +160,10 @@ int gemv_launch(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const float
     const int64_t nsteps = (K + Bf16::kStepElems - 1) / Bf16::kStepElems;
     if (nsteps > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
     Bf16::Args a;
-    a.c = sg::make_common(M, static_cast<int>(nsteps), R, di.sm_count);
-    if (static_cast<int64_t>(a.c.nseg) * R > sg::kMaxPartials) return WSW_ERR_UNSUPPORTED;
+    a.c = sg::make_common(M, static_cast<int>(nsteps), R, di.sm_count, Bf16::kWarps);
     a.W = W; a.K = K; a.ld = ld; a.x = x; a.alpha = alpha; a.y = y;
-    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 2;
-    const unsigned ctas = static_cast<unsigned>(di.sm_count * cps);
+    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 16 / Bf16::kWarps;
+    const unsigned ctas = sg::grid_ctas(a.c, static_cast<int64_t>(di.sm_count) * cps);
     const bool xs = nsteps <= kMaxSmemSteps;
     const size_t x_smem = xs ? static_cast<size_t>(nsteps) * 2048 : 0;
     const int lb = load_width(W, ld * 2, o.load_bytes);

@@ -14,9 +14,9 @@
 // agree bit for bit): a lane owns whole blocks, block 32*s + lane in step s of a row
 // (one 256-bit load of 32 int8 values); the exact block sum comes from eight dp4a; the
 // lane multiplies the exact fp32 product Wd*xd by it and accumulates with an fp32 FMA,
-// its blocks in increasing order; at the end of each K-segment of two steps a
-// xor-butterfly reduces the lanes, and the segment sums are added first to last (the
-// work decomposition is in stream_gemv.cuh).
+// its blocks in increasing order; at the end of each K-segment a xor-butterfly reduces
+// the lanes, and the segment sums are added first to last (the segments and the work
+// decomposition are in stream_gemv.cuh).
 #include <cuda_fp16.h>
 
 #include "moe_tc.cuh"
@@ -60,6 +60,7 @@ __device__ __forceinline__ float warp_sum(float s) {
 // ---------------------------------------------------------------- dense ----
 
 struct Q8 {
+    static constexpr int kWarps = 8;  // warps per CTA
     static constexpr int kStepElems = 1024;
     static constexpr bool kGlobalX = false;  // x is always staged in shared memory
     struct Args {
@@ -71,6 +72,10 @@ struct Q8 {
         const uint16_t *xd;
         float *y;
     };
+    __device__ __forceinline__ static const char *row_ptr(const Args &a, int64_t row) {
+        return reinterpret_cast<const char *>(a.Wq + row * a.ldq);
+    }
+    __device__ __forceinline__ static int64_t row_bytes(const Args &a) { return a.K; }
     struct Buf { uint32_t w[8]; uint32_t d; };
     struct Acc { float a; };
     struct XVal { uint4 x0, x1; uint32_t d; };
@@ -93,12 +98,6 @@ struct Q8 {
         for (int i = 0; i < 8; ++i) b.w[i] = 0u;
         b.d = 0u;
     }
-    __device__ __forceinline__ static void prefetch(const Args &a, int64_t row, int step, int lane) {
-        const char *p = reinterpret_cast<const char *>(a.Wq + row * a.ldq);
-        const int64_t end = a.K;
-        int64_t begin = static_cast<int64_t>(step) * 1024 + 4096;
-        for (int64_t off = begin + lane * 128; off < end && off < begin + 8192; off += 32 * 128) prefetch_l2(p + off);
-    }
     // Shared memory: xq as two planes of 16-byte halves [2][nsteps * 32], then xd.
     template <bool XS>
     __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
@@ -107,7 +106,7 @@ struct Q8 {
         uint16_t *xs_d = reinterpret_cast<uint16_t *>(xs + 2 * nslots);
         const int64_t nblk = a.K / 32;
         const bool xvec = (reinterpret_cast<uintptr_t>(a.xq) & 15) == 0;
-        for (int64_t h = threadIdx.x; h < 2 * nslots; h += sg::kThreads) {
+        for (int64_t h = threadIdx.x; h < 2 * nslots; h += blockDim.x) {
             // half h = bytes 16h .. 16h+15 = plane (h & 1) of block h >> 1
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (16 * h < a.K) {
@@ -122,7 +121,7 @@ struct Q8 {
             }
             xs[(h & 1) * nslots + (h >> 1)] = v;
         }
-        for (int64_t b = threadIdx.x; b < nslots; b += sg::kThreads) xs_d[b] = b < nblk ? a.xd[b] : 0;
+        for (int64_t b = threadIdx.x; b < nslots; b += blockDim.x) xs_d[b] = b < nblk ? a.xd[b] : 0;
     }
     template <bool XS>
     __device__ __forceinline__ static XVal load_x(const Args &, const unsigned char *xsm, int step, int lane,
@@ -174,7 +173,7 @@ struct MoeArgs {
     float *y;
     int32_t *err;
     int nsteps;     // ceil(K / 1024)
-    int seg_steps;  // as the dense kernel on one expert's Mo x K matrix
+    int log2_seg;   // K-segments (log2) as the dense kernel on one expert's Mo x K matrix
     int xs_cap;     // activation rows that fit the shared-memory staging area
     int64_t xs_off; // byte offset of that area in dynamic shared memory
 };
@@ -362,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gemv_q8_0_kernel(const MoeArg
     };
 
     int m[kMoeNT];
+    int cseg = 0;   // K-segment of the compute cursor's step
     int slot0 = 0;  // staging slot of the unit's first row (rows of a batch are consecutive)
     float acc[kMoeNT], tot[kMoeNT];
     auto load_tokens = [&]() {
@@ -383,8 +383,10 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gemv_q8_0_kernel(const MoeArg
                 const int s = cc.st;
                 const int64_t b = static_cast<int64_t>(s) * 32 + lane;
                 const bool valid = b < nblk;
-                const bool seg_end = ((s + 1) % a.seg_steps == 0) || (s + 1 == nsteps);
-                const int seg = s / a.seg_steps;
+                if (s == 0) cseg = 0;
+                const bool seg_end = s + 1 == sg::seg_begin(cseg + 1, nsteps, a.log2_seg);
+                const int seg = cseg;
+                if (seg_end) ++cseg;
 #pragma unroll
                 for (int t = 0; t < kMoeNT; ++t) {
                     if (m[t] < 0) continue;  // warp-uniform
@@ -469,11 +471,10 @@ extern "C" int wsw_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, in
     const int64_t nsteps = (K + Q8::kStepElems - 1) / Q8::kStepElems;
     if (nsteps > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
     Q8::Args a;
-    a.c = sg::make_common(M, static_cast<int>(nsteps), R, di.sm_count);
-    if (static_cast<int64_t>(a.c.nseg) * R > sg::kMaxPartials) return WSW_ERR_UNSUPPORTED;
+    a.c = sg::make_common(M, static_cast<int>(nsteps), R, di.sm_count, Q8::kWarps);
     a.Wq = Wq; a.Wd = Wd; a.K = K; a.ldq = ldq; a.xq = xq; a.xd = xd; a.y = y;
-    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 2;
-    const unsigned ctas = static_cast<unsigned>(di.sm_count * cps);
+    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 16 / Q8::kWarps;
+    const unsigned ctas = sg::grid_ctas(a.c, static_cast<int64_t>(di.sm_count) * cps);
     const size_t x_smem = static_cast<size_t>(nsteps) * (1024 + 64);
     if (sg::kMaxPartials * 4 + x_smem > static_cast<size_t>(di.max_smem_optin)) return WSW_ERR_UNSUPPORTED;
     const int lb = load_width(Wq, ldq, o.load_bytes);
@@ -512,7 +513,7 @@ extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E
     a.Wq = Wq; a.Wd = Wd; a.E = E; a.Mo = Mo; a.K = K; a.xq = xq; a.xd = xd; a.ids = ids; a.R = R;
     a.y = y; a.err = err_flag;
     a.nsteps = static_cast<int>((K + Q8::kStepElems - 1) / Q8::kStepElems);
-    a.seg_steps = sg::choose_seg_steps(Mo, a.nsteps, di.sm_count);
+    a.log2_seg = sg::choose_log2_seg(Mo, a.nsteps, di.sm_count, Q8::kWarps);
     // cnt, off, cur, nbt, ubase[E+1] (int64), used, list, then the activation staging area
     const size_t base_smem = (static_cast<size_t>(4 * E) * sizeof(int) + static_cast<size_t>(E + 1) * 8 +
                               static_cast<size_t>(E + R) * sizeof(int) + 15) & ~static_cast<size_t>(15);
