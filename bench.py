@@ -6,16 +6,19 @@ int8 blocks with fp16 scales, quantized from N(0, 0.02) bf16) at batch 1, with t
 activation x (length 4096, N(0,1)) quantized to q8_0 in front of it, and the
 256-element superblock quantizer on x (length 4096) and on y (length 14336).
 
-  token  = quantize_q8(x_t, 32) -> gemv_q8_0(W_{t mod 16}, x_t), PDL-linked on the main
-           stream; quantize_q8(x_t, 256) and quantize_q8(y_t, 256) on a side stream
-           that forks after the GEMV (they overlap the next token's chain).
+  token  = quantize_gemv_q8_0(W_{t mod 16}, x_t): one launch that quantizes x_t to q8_0
+           (writing q and d out) and runs the mat-vec, PDL-linked to the previous
+           token on the main stream; quantize_q8(x_t, 256) and quantize_q8(y_t, 256) on
+           a side stream that forks after it (they overlap the next token's chain).
+           The same step with the quantizer as its own launch (quantize_q8 ->
+           gemv_q8_0) is timed too and reported as "two_launch_step".
   step   = a batch of 2048 tokens (distinct synthetic activations), captured once in
            a CUDA graph and replayed.  16 distinct weight copies (1.0 GB) rotate, so
            every GEMV streams weights that are not in the 129 MB L2.
   value  = algorithmic bytes of the step / step time (GB/s), summed over ranks.
 
-The same line also reports: the GEMV kernel alone against the HBM roofline (CUDA
-events over back-to-back launches on distinct weight copies), the batch-1 quantizer
+The same line also reports: the fused quantize + GEMV kernel against the HBM roofline
+(CUDA events over back-to-back launches on distinct weight copies), the GEMV alone, the batch-1 quantizer
 in us/call (graph-amortised over 1000 calls), the 27B-shaped bf16 decode chain
 (64 layers x [QKV, O, gate/up, down] + lm_head, 257 PDL-linked mat-vecs, 43.16 GB
 per token), the end-to-end rate through the C ABI with host buffers, and the CPU
@@ -53,7 +56,9 @@ B_Q32 = K * 4 + K + (K // 32) * 2                       # x in, q out, fp16 scal
 B_GEMV = M * K + M * (K // 32) * 2 + K + (K // 32) * 2 + M * 4
 B_Q256_Y = M * 4 + M + (M // 256) * 4
 B_Q256_X = K * 4 + K + (K // 256) * 4
-B_TOKEN = B_Q32 + B_GEMV + B_Q256_Y + B_Q256_X
+B_TOKEN_2L = B_Q32 + B_GEMV + B_Q256_Y + B_Q256_X          # quantizer as its own launch
+B_FUSED = B_GEMV - K - (K // 32) * 2 + K * 4 + K + (K // 32) * 2  # x in, q and d out, no re-read
+B_TOKEN = B_FUSED + B_Q256_Y + B_Q256_X
 
 CHAIN_LAYER = [(6144, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
 CHAIN_HEAD = (152064, 5120)
@@ -171,13 +176,17 @@ class Workload:
         self.wq = [w.data_ptr() for w in self.Wq]
         self.wd = [w.data_ptr() for w in self.Wd]
 
-    def token(self, t, stream, side, rc):
+    def token(self, t, stream, side, rc, fused=True):
         L, p, o = self.L, self.ptr, self.popts
         x = p["X"] + t * K * 4
         xq, xd = p["xq"] + t * K, p["xd"] + t * (K // 32) * 2
         y = p["Y"] + t * M * 4
-        rc |= L.wsw_quantize_q8(x, 1, K, K, 32, xq, xd, stream, o)
-        rc |= L.wsw_gemv_q8_0(self.wq[t % NCOPY], self.wd[t % NCOPY], M, K, K, xq, xd, y, stream, o)
+        if fused:
+            rc |= L.wsw_quantize_gemv_q8_0(self.wq[t % NCOPY], self.wd[t % NCOPY], M, K, K, x, xq, xd, y,
+                                           stream, o)
+        else:
+            rc |= L.wsw_quantize_q8(x, 1, K, K, 32, xq, xd, stream, o)
+            rc |= L.wsw_gemv_q8_0(self.wq[t % NCOPY], self.wd[t % NCOPY], M, K, K, xq, xd, y, stream, o)
         if side is None:
             rc |= L.wsw_quantize_q8(y, 1, M, M, 256, p["yq"] + t * M, p["ys"] + t * (M // 256) * 4, stream, o)
             rc |= L.wsw_quantize_q8(x, 1, K, K, 256, p["xq2"] + t * K, p["xs2"] + t * (K // 256) * 4, stream, o)
@@ -190,7 +199,7 @@ class Workload:
             rc |= L.wsw_quantize_q8(x, 1, K, K, 256, p["xq2"] + t * K, p["xs2"] + t * (K // 256) * 4, sp, o)
         return rc
 
-    def step(self, stream, overlap=True):
+    def step(self, stream, overlap=True, fused=True):
         """One batch of TOKENS decode tokens on `stream`; with overlap the
         superblock quantizations go to a side stream joined at the end."""
         torch = self.torch
@@ -205,7 +214,7 @@ class Workload:
             side = (self._ev, self._side)
             self._side.wait_stream(main)
         for t in range(TOKENS):
-            rc = self.token(t, stream, side, rc)
+            rc = self.token(t, stream, side, rc, fused)
         if side is not None:
             main.wait_stream(self._side)
         if rc:
@@ -236,7 +245,8 @@ def _time_graph(torch, g, reps):
     return e0.elapsed_time(e1) / 1000.0 / reps
 
 
-KERNEL_SOURCES = {"gemv_q8_0": ("gemv_q8_0.cu", "stream_gemv.cuh", "common.cuh")}
+KERNEL_SOURCES = {"gemv_q8_0": ("gemv_q8_0.cu", "stream_gemv.cuh", "common.cuh"),
+                  "quantize_gemv_q8_0": ("gemv_q8_0.cu", "stream_gemv.cuh", "q8_math.cuh", "common.cuh")}
 
 
 def kernel_source_sha(name):
@@ -260,15 +270,23 @@ def _traffic_record(name):
     return None
 
 
-def measure_gemv_kernel(torch, wl):
-    """gemv_q8_0 alone: 256 back-to-back PDL launches over the 16 weight copies."""
+def measure_gemv_kernel(torch, wl, fused=True):
+    """The fused quantize + GEMV (or gemv_q8_0 alone): 256 back-to-back PDL launches
+    over the 16 weight copies."""
     n = 256
 
     def fn(stream):
         rc = 0
         for i in range(n):
-            rc |= wl.L.wsw_gemv_q8_0(wl.wq[i % NCOPY], wl.wd[i % NCOPY], M, K, K, wl.ptr["xq"], wl.ptr["xd"],
-                                     wl.ptr["Y"] + (i % 64) * M * 4, stream, wl.popts)
+            t = i % 64
+            if fused:
+                rc |= wl.L.wsw_quantize_gemv_q8_0(wl.wq[i % NCOPY], wl.wd[i % NCOPY], M, K, K,
+                                                  wl.ptr["X"] + t * K * 4, wl.ptr["xq"] + t * K,
+                                                  wl.ptr["xd"] + t * (K // 32) * 2, wl.ptr["Y"] + t * M * 4,
+                                                  stream, wl.popts)
+            else:
+                rc |= wl.L.wsw_gemv_q8_0(wl.wq[i % NCOPY], wl.wd[i % NCOPY], M, K, K, wl.ptr["xq"],
+                                         wl.ptr["xd"], wl.ptr["Y"] + t * M * 4, stream, wl.popts)
         assert rc == 0
 
     g = _graph(torch, fn)
@@ -526,9 +544,17 @@ def run_ours(args):
     step_s = elapsed / args.steps
     value = B_TOKEN * TOKENS * world / step_s / 1e9
 
+    # the same step with the quantizer as its own launch
+    two_graph = _graph(torch, lambda stream: wl.step(stream, fused=False))
+    for _ in range(2):
+        two_graph.replay()
+    two_s = statistics.median(_time_graph(torch, two_graph, 1) for _ in range(5))
+    del two_graph
+
     peak, peak_kind = _peaks()
     k_med, k_min, k_max = measure_gemv_kernel(torch, wl)
-    achieved = B_GEMV / k_med / 1e9
+    achieved = B_FUSED / k_med / 1e9
+    g_med, _, _ = measure_gemv_kernel(torch, wl, fused=False)
     quant = measure_quantizer(torch, wl)
     e2e = measure_e2e(torch, wl, dev, args.steps)
     del step_graph
@@ -555,8 +581,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "int8 x int8 -> int32 blocks, fp32 scale/accumulate (q8_0); fp32 quantizer",
         "data": "synthetic: seeded N(0,0.02) bf16 weights quantized to q8_0, N(0,1) activations",
-        "config": {"workload": "q8_0 decode GEMV 14336x4096 batch 1 + q8_0 quantizer (n=4096) + "
-                               "superblock quantizer (n=4096, n=14336), PDL-linked",
+        "config": {"workload": "q8_0 decode GEMV 14336x4096 batch 1 + q8_0 quantizer (n=4096, fused into "
+                               "the GEMV launch) + superblock quantizer (n=4096, n=14336), PDL-linked",
                    "tokens_per_step": TOKENS, "bytes_per_token": B_TOKEN,
                    "weight_copies": NCOPY, "weight_bytes_per_copy": B_GEMV - K - (K // 32) * 2 - M * 4,
                    "l2": "inputs larger than L2: 16 rotating weight copies (1.0 GB) vs 129 MB L2",
@@ -565,17 +591,24 @@ def run_ours(args):
         "pct_of_measured_hbm_peak": round(100.0 * value / world / peak, 2),
         "pct_of_nominal_8TBps": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "quantizer_us_per_call": quant,
-        "roofline": {"kernel": "gemv_q8_0_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": "stream_gemv_kernel<Q8X> (quantize_gemv_q8_0)", "bound": "hbm",
+                     "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": _traffic_record("gemv_q8_0"),
-                     "algorithmic_bytes_per_launch": B_GEMV,
+                     "traffic": _traffic_record("quantize_gemv_q8_0"),
+                     "algorithmic_bytes_per_launch": B_FUSED,
                      "launch_us": {"median": round(k_med * 1e6, 3), "min": round(k_min * 1e6, 3),
                                    "max": round(k_max * 1e6, 3)}},
+        "gemv_q8_0_alone": {"GBps": round(B_GEMV / g_med / 1e9, 1), "frac": round(B_GEMV / g_med / 1e9 / peak, 4),
+                            "launch_us": round(g_med * 1e6, 3), "traffic": _traffic_record("gemv_q8_0"),
+                            "algorithmic_bytes_per_launch": B_GEMV},
+        "two_launch_step": {"GBps": round(B_TOKEN_2L * TOKENS / two_s / 1e9, 2),
+                            "ms_per_step": round(two_s * 1e3, 4),
+                            "note": "quantize_q8 -> gemv_q8_0 as two PDL-linked launches per token"},
         "chain_27b_bf16": chain,
         "rows": rows,
         "e2e": e2e,
-        "gpu_launches": 4 * TOKENS * args.steps,
+        "gpu_launches": 3 * TOKENS * args.steps,
         "clocks": clk,
         "cpu_baseline": None if cpu_v is None else {
             "value": round(cpu_v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",

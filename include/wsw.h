@@ -161,6 +161,24 @@ int wsw_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, int64_t K, in
                   const wsw_launch_opts *opts);
 
 /*
+ * wsw_quantize_gemv_q8_0 -- the batch-1 decode step of [P3] Scope (quantize the
+ * activation to q8_0, then the quantized mat-vec) in one launch: every CTA quantizes
+ * the fp32 x itself while its first weight loads are in flight, so no separate
+ * quantizer kernel sits between two chained mat-vecs.
+ *
+ *   y = wsw_gemv_q8_0(Wq, Wd, M, K, ldq, q(x), d(x))  with (q(x), d(x)) =
+ *       wsw_quantize_q8(x, 1, K, K, 32), bit for bit.
+ *
+ *   Wq, Wd, M, K, ldq, y   as wsw_gemv_q8_0.
+ *   x        fp32 [K], 4-byte aligned.
+ *   xq_out   int8 [K] and xd_out binary16 [K/32]: both NULL, or both set to receive
+ *            the quantized activation (the bytes wsw_quantize_q8 writes).
+ */
+int wsw_quantize_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, int64_t K, int64_t ldq,
+                           const float *x, int8_t *xq_out, uint16_t *xd_out, float *y, void *stream,
+                           const wsw_launch_opts *opts);
+
+/*
  * wsw_moe_gemv_q8_0 -- grouped MoE mat-vec over per-expert q8_0 weights ([P3]
  * Cause and Scope: the MoE path quantizes m = T x top_k rows, then runs a grouped
  * GEMM over the experts).
@@ -179,7 +197,7 @@ int wsw_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, int64_t K, in
  *        row is left untouched, and *err_flag (if err_flag != NULL) is set to a
  *        nonzero value.  The library never clears *err_flag.
  *   y    fp32 [R][Mo].
- *   R <= 65536.
+ *   R <= 16384 and E <= 1024, else WSW_ERR_UNSUPPORTED.
  */
 int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E, int64_t Mo, int64_t K,
                       const int8_t *xq, const uint16_t *xd, const int32_t *ids, int64_t R,

@@ -81,6 +81,12 @@ def test_gemv_rejects_on_host(lib):
     assert g(P(4096), P(4096), 4, 64, 80, P(4096), P(4096), P(4096), None, None) == INVALID  # ldq % 32
     assert g(P(4096), P(4096), 4, 64, 32, P(4096), P(4096), P(4096), None, None) == INVALID  # ldq < K
     assert g(P(4096), P(4097), 4, 64, 64, P(4096), P(4096), P(4096), None, None) == MISALIGNED
+    q = lib.wsw_quantize_gemv_q8_0
+    assert q(P(4096), P(4096), 4, 48, 64, P(4096), None, None, P(4096), None, None) == INVALID  # K % 32
+    assert q(P(4096), P(4096), 4, 64, 64, P(4096), P(4096), None, P(4096), None, None) == INVALID  # xq without xd
+    assert q(P(4096), P(4096), 4, 64, 64, None, None, None, P(4096), None, None) == INVALID  # no x
+    assert q(P(4096), P(4096), 4, 64, 64, P(4098), None, None, P(4096), None, None) == MISALIGNED  # x
+    assert q(P(4096), P(4096), 0, 64, 64, P(4096), None, None, None, None, None) == 0
 
 
 def test_other_calls_reject_on_host(lib):

@@ -108,3 +108,66 @@ def test_degenerate_sizes():
                       torch.zeros((4, 1), dtype=torch.float16, device="cuda"),
                       torch.zeros(48, dtype=torch.int8, device="cuda"),
                       torch.zeros(1, dtype=torch.float16, device="cuda"))
+
+
+# ------------------------------------------------ quantizer fused into the GEMV ----
+
+def _fused_vs_two_calls(wsw, Wqd, Wdd, x, opts=None):
+    """The fused call against quantize_q8 followed by gemv_q8_0: y, xq and xd all bit
+    for bit; returns the quantized activation."""
+    K = x.numel()
+    xq_ref, xd_ref = wsw.quantize_q8(x, 32)
+    y_ref = wsw.gemv_q8_0(Wqd, Wdd, xq_ref, xd_ref, K=K)
+    xq = torch.full((K,), 99, dtype=torch.int8, device="cuda")
+    xd = torch.full((K // 32,), 7.0, dtype=torch.float16, device="cuda")
+    y = wsw.quantize_gemv_q8_0(Wqd, Wdd, x, K=K, x_out=(xq, xd), opts=opts)
+    assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32))
+    assert torch.equal(xq, xq_ref) and torch.equal(xd.view(torch.int16), xd_ref.view(torch.int16))
+    return y, xq, xd
+
+
+def test_fused_quantize_gemv_config(orc, cfg2):
+    """14336 x 4096: the fused call equals the two calls bit for bit, its quantized x
+    equals the oracle's bytes, and y is within 1e-4 of the fp64 oracle."""
+    wsw = need_gpu()
+    Wq, Wd, _, _ = cfg2
+    x = syn.normal(0, "xq4096", (1, 4096))
+    Wqd, Wdd = torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda()
+    y, xq, xd = _fused_vs_two_calls(wsw, Wqd, Wdd, x.cuda()[0], opts={"pdl": 1})
+    xqr, xdr = orc.quantize_q8(x.numpy(), 32)
+    assert (xq.cpu().numpy() == xqr[0]).all() and (f16_bits(xd) == xdr[0]).all()
+    check_tol(y.cpu().numpy(), orc.gemv_q8_0(Wq, Wd, xqr[0], xdr[0]), mag_q8(Wq, Wd, xqr[0], xdr[0]), TOL_Q8, "fused")
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (17, 544), (3, 4128), (65, 768), (257, 2048), (8, 8192), (4000, 14336)])
+def test_fused_ragged_shapes_and_knobs(orc, M, K):
+    wsw = need_gpu()
+    Wq, Wd, _, _ = _make(orc, 2, M, K)
+    Wqd, Wdd = torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda()
+    x = syn.normal(2, "fx%d" % K, (K,)).cuda()
+    x[32:64] = 0.0  # an all-zero block (d = +0, q = 0) when K > 32
+    for opts in (None, dict(rows_per_warp=1, load_bytes=8, pdl=0), dict(rows_per_warp=4, load_bytes=16)):
+        _fused_vs_two_calls(wsw, Wqd, Wdd, x, opts)
+    # x at an address that is 4- but not 16-byte aligned: scalar loads, same bytes
+    buf = torch.zeros(K + 1, device="cuda")
+    buf[1:] = x
+    _fused_vs_two_calls(wsw, Wqd, Wdd, buf[1:])
+
+
+def test_fused_without_outputs_and_degenerate():
+    wsw = need_gpu()
+    M, K = 300, 1024
+    g = torch.Generator(device="cuda").manual_seed(3)
+    Wqd = torch.randint(-127, 128, (M, K), dtype=torch.int8, device="cuda", generator=g)
+    Wdd = (torch.rand((M, K // 32), device="cuda", generator=g) * 1e-2).half()
+    x = torch.randn(K, device="cuda", generator=g)
+    y = wsw.quantize_gemv_q8_0(Wqd, Wdd, x)
+    y_ref = wsw.gemv_q8_0(Wqd, Wdd, *wsw.quantize_q8(x, 32))
+    assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32))
+    # no rows: only the quantized activation is produced
+    xq = torch.empty(K, dtype=torch.int8, device="cuda")
+    xd = torch.empty(K // 32, dtype=torch.float16, device="cuda")
+    y0 = wsw.quantize_gemv_q8_0(Wqd[:0], Wdd[:0], x, x_out=(xq, xd))
+    assert y0.numel() == 0
+    xq_ref, xd_ref = wsw.quantize_q8(x, 32)
+    assert torch.equal(xq, xq_ref) and torch.equal(xd.view(torch.int16), xd_ref.view(torch.int16))

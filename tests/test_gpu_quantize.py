@@ -61,6 +61,46 @@ def test_quantize_ties_and_exact_grid(orc):
     assert q[0, 32:64].tolist() == k.int().tolist()
 
 
+def _near_tie_blocks(block, nblocks, seed):
+    """Blocks whose first value is the amax and whose other values sit on, or a few
+    ulps around, the half-integer multiples (n + 1/2) d of the block's scale
+    d = fp32(amax / 127): the values where rounding v / d to an integer is decided in
+    the last bits of the quotient."""
+    rng = np.random.default_rng(seed)
+    x = np.zeros((nblocks, block), np.float32)
+    for b in range(nblocks):
+        amax = np.float32(10.0 ** rng.uniform(-20, 20))
+        d = np.float32(amax) / np.float32(127.0)
+        n = rng.integers(-127, 127, block - 1)
+        v = ((n + 0.5) * np.float64(d)).astype(np.float32)
+        for k in range(block - 1):
+            for _ in range(abs(int(rng.integers(-8, 9)))):
+                v[k] = np.nextafter(v[k], np.float32(np.inf) if k % 2 else np.float32(-np.inf))
+        v = np.clip(v, -amax, amax)
+        x[b, 0] = amax if b % 2 else -amax
+        x[b, 1:] = v
+    return torch.from_numpy(x.reshape(1, -1))
+
+
+@pytest.mark.parametrize("block", [32, 256])
+def test_quantize_near_ties_against_oracle(orc, block):
+    """Values on and around the rounding boundaries of x / d, over scales 1e-20 ..
+    1e20: the codes equal the oracle's (exact fp32 division) bit for bit, in the
+    quantizer and in the mat-vec that quantizes its own activation."""
+    wsw = need_gpu()
+    x = _near_tie_blocks(block, 4096 // block * 16, block)
+    _compare(wsw, orc, x, block)
+    if block == 32:
+        n = x.shape[1]
+        xr, dr = orc.quantize_q8(x.numpy(), 32)
+        xq = torch.empty(n, dtype=torch.int8, device="cuda")
+        xd = torch.empty(n // 32, dtype=torch.float16, device="cuda")
+        Wq = torch.ones((8, n), dtype=torch.int8, device="cuda")
+        Wd = torch.ones((8, n // 32), dtype=torch.float16, device="cuda")
+        wsw.quantize_gemv_q8_0(Wq, Wd, x.cuda()[0], x_out=(xq, xd))
+        assert (xq.cpu().numpy() == xr[0]).all() and (f16_bits(xd) == dr[0]).all()
+
+
 @pytest.mark.parametrize("block", [32, 256])
 def test_quantize_moe_batch_shape(orc, block):
     """T = 512 tokens x top_k 8 rows of the 2048-wide hidden state."""

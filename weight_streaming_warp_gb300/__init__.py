@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "LaunchOpts", "WswError", "library_path", "load", "quantize_q8", "gemv_bf16",
-    "gemv_bf16_chain", "gemv_q8_0", "moe_gemv_q8_0", "dequant_q8_0_kv", "gemm_bf16",
+    "gemv_bf16_chain", "gemv_q8_0", "quantize_gemv_q8_0", "moe_gemv_q8_0", "dequant_q8_0_kv", "gemm_bf16",
     "upload_padded", "status_string", "abi_version",
 ]
 
@@ -77,10 +77,11 @@ def load():
     L.wsw_gemv_bf16.argtypes = [_p, _i64, _i64, _i64, _p, _f32, _p, _p, _p]
     L.wsw_gemv_bf16_chain.argtypes = [_i64, _p, _p, _p]
     L.wsw_gemv_q8_0.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p]
+    L.wsw_quantize_gemv_q8_0.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p]
     L.wsw_moe_gemv_q8_0.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p, _i64, _p, _p, _p, _p]
     L.wsw_dequant_q8_0_kv.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p]
     L.wsw_gemm_bf16.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _p, _p]
-    for f in ("wsw_quantize_q8", "wsw_gemv_bf16", "wsw_gemv_bf16_chain", "wsw_gemv_q8_0",
+    for f in ("wsw_quantize_q8", "wsw_gemv_bf16", "wsw_gemv_bf16_chain", "wsw_gemv_q8_0", "wsw_quantize_gemv_q8_0",
               "wsw_moe_gemv_q8_0", "wsw_dequant_q8_0_kv", "wsw_gemm_bf16"):
         getattr(L, f).restype = ctypes.c_int
     _lib = L
@@ -187,6 +188,26 @@ def gemv_q8_0(Wq, Wd, xq, xd, K=None, out=None, opts=None):
     y = torch.empty(M, dtype=torch.float32, device=Wq.device) if out is None else out
     _check(load().wsw_gemv_q8_0(Wq.data_ptr(), Wd.data_ptr(), M, K, ldq, xq.data_ptr(), xd.data_ptr(),
                                 y.data_ptr(), _stream(), _opts(opts)), "gemv_q8_0")
+    return y
+
+
+def quantize_gemv_q8_0(Wq, Wd, x, K=None, out=None, x_out=None, opts=None):
+    """y fp32 [M] from q8_0 weights and the fp32 activation x [K], quantized to q8_0
+    (block 32) inside the same launch; equals gemv_q8_0(Wq, Wd, *quantize_q8(x, 32))
+    bit for bit.  x_out = (xq int8 [K], xd fp16 [K/32]) receives the quantized x."""
+    _dev(Wq, torch.int8, "Wq")
+    _dev(Wd, torch.float16, "Wd")
+    _dev(x, torch.float32, "x")
+    M, cols, ldq = _rowmajor(Wq, "Wq")
+    K = cols if K is None else int(K)
+    y = torch.empty(M, dtype=torch.float32, device=Wq.device) if out is None else out
+    xq_p = xd_p = None
+    if x_out is not None:
+        _dev(x_out[0], torch.int8, "xq_out")
+        _dev(x_out[1], torch.float16, "xd_out")
+        xq_p, xd_p = x_out[0].data_ptr(), x_out[1].data_ptr()
+    _check(load().wsw_quantize_gemv_q8_0(Wq.data_ptr(), Wd.data_ptr(), M, K, ldq, x.data_ptr(), xq_p, xd_p,
+                                         y.data_ptr(), _stream(), _opts(opts)), "quantize_gemv_q8_0")
     return y
 
 

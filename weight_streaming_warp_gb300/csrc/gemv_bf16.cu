@@ -160,7 +160,7 @@ int gemv_launch(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const float
     const int64_t nsteps = (K + Bf16::kStepElems - 1) / Bf16::kStepElems;
     if (nsteps > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
     Bf16::Args a;
-    a.c = sg::make_common(M, static_cast<int>(nsteps), R, di.sm_count, Bf16::kWarps);
+    a.c = sg::make_common(M, static_cast<int>(nsteps), R, di.sm_count, Bf16::kWarps, Bf16::kWarps);
     a.W = W; a.K = K; a.ld = ld; a.x = x; a.alpha = alpha; a.y = y;
     const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 16 / Bf16::kWarps;
     const unsigned ctas = sg::grid_ctas(a.c, static_cast<int64_t>(di.sm_count) * cps);

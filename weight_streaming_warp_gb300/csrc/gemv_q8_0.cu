@@ -20,6 +20,7 @@
 #include <cuda_fp16.h>
 
 #include "moe_tc.cuh"
+#include "q8_math.cuh"
 #include "stream_gemv.cuh"
 
 namespace wsw {
@@ -143,6 +144,96 @@ struct Q8 {
     __device__ __forceinline__ static float lane_total(const Acc &c) { return c.a; }
     __device__ __forceinline__ static void store(const Args &a, int64_t row, float s) { a.y[row] = s; }
 };
+
+// The dense mat-vec whose CTAs quantize the fp32 activation themselves, with the
+// quantizer's block arithmetic (q8_math.cuh): y equals wsw_quantize_q8 (block 32)
+// followed by wsw_gemv_q8_0, bit for bit, and the quantizer is off the critical path
+// of a decode chain.  CTA 0 can also write the quantized activation out.
+struct Q8X : Q8 {
+    static constexpr int kWarps = 16;  // one CTA per SM: x is quantized once per SM
+    struct Args : Q8::Args {
+        const float *x;
+        int8_t *xq_out;    // optional (with xd_out): q of x, K bytes
+        uint16_t *xd_out;  // optional: binary16 scales, K / 32
+    };
+    template <bool XS>
+    __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
+        constexpr int kB = 2;  // passes whose x loads are in flight together
+        const int64_t nslots = static_cast<int64_t>(nsteps) * 32;
+        uint16_t *xs_d = reinterpret_cast<uint16_t *>(xsm + 32 * nslots);
+        const bool xvec = (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
+        const bool out = blockIdx.x == 0 && a.xq_out != nullptr;
+        const bool ovec = (reinterpret_cast<uintptr_t>(a.xq_out) & 7) == 0;
+        const int64_t nt = 4 * nslots;  // a multiple of 128: whole warps iterate together
+        // Thread t quantizes values 8t .. 8t+7, quarter (t & 3) of block t >> 2 (block
+        // amax uses shuffles, so every lane of a warp runs every pass).  Blocks past K
+        // are zero: d = +0 and q = 0, as the padding of Q8.
+        for (int64_t t0 = threadIdx.x; t0 < nt; t0 += kB * static_cast<int64_t>(blockDim.x)) {
+            float v[kB][8];
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int64_t e0 = 8 * (t0 + u * static_cast<int64_t>(blockDim.x));
+                if (e0 < a.K) {  // K % 32 == 0: a block is entirely inside or outside
+                    if (xvec) {
+                        const float4 p = __ldg(reinterpret_cast<const float4 *>(a.x + e0));
+                        const float4 q = __ldg(reinterpret_cast<const float4 *>(a.x + e0) + 1);
+                        v[u][0] = p.x; v[u][1] = p.y; v[u][2] = p.z; v[u][3] = p.w;
+                        v[u][4] = q.x; v[u][5] = q.y; v[u][6] = q.z; v[u][7] = q.w;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) v[u][i] = __ldg(a.x + e0 + i);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[u][i] = 0.0f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int64_t t = t0 + u * static_cast<int64_t>(blockDim.x);
+                const float amax = q8m::block_amax<32>(v[u]);
+                if (t >= nt) continue;  // warp-uniform
+                const float d = q8m::scale(amax);
+                uint32_t p[2];
+                q8m::codes(v[u], amax, d, p);
+                const int64_t b = t >> 2;
+                const int qt = static_cast<int>(t & 3);
+                // bytes 8 qt .. 8 qt + 7 of block b: plane qt >> 1, offset 8 (qt & 1)
+                *reinterpret_cast<uint2 *>(xsm + ((qt >> 1) * nslots + b) * 16 + 8 * (qt & 1)) = make_uint2(p[0], p[1]);
+                const uint16_t dbits = __half_as_ushort(__float2half_rn(d));
+                if (qt == 0) xs_d[b] = dbits;
+                const int64_t e0 = 8 * t;
+                if (out && e0 < a.K) {
+                    if (ovec) {
+                        *reinterpret_cast<uint2 *>(a.xq_out + e0) = make_uint2(p[0], p[1]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            a.xq_out[e0 + i] = static_cast<int8_t>((p[i >> 2] >> (8 * (i & 3))) & 0xffu);
+                    }
+                    if (qt == 0) a.xd_out[b] = dbits;
+                }
+            }
+        }
+    }
+};
+
+// Dense launch shared by the two entry points (arguments already validated).
+template <class F>
+int q8_dense_launch(typename F::Args &a, int64_t M, int64_t K, const Opts &o, const DeviceInfo &di,
+                    cudaStream_t s) {
+    const int R = o.rows_per_warp;
+    const int64_t nsteps = (K + Q8::kStepElems - 1) / Q8::kStepElems;
+    if (nsteps > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
+    a.c = sg::make_common(M, static_cast<int>(nsteps), R, di.sm_count, F::kWarps, Q8::kWarps);
+    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 16 / F::kWarps;
+    const unsigned ctas = sg::grid_ctas(a.c, static_cast<int64_t>(di.sm_count) * cps);
+    const size_t x_smem = static_cast<size_t>(nsteps) * (1024 + 64);
+    if (sg::kMaxPartials * 4 + x_smem > static_cast<size_t>(di.max_smem_optin)) return WSW_ERR_UNSUPPORTED;
+    const int lb = load_width(a.Wq, a.ldq, o.load_bytes);
+    const cudaError_t e = sg::launch_stream_gemv<F>(R, lb, true, a, ctas, x_smem, s, o.pdl);
+    return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
+}
 
 // ---------------------------------------------------------------- grouped ---
 //
@@ -467,19 +558,44 @@ extern "C" int wsw_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, in
     if (K == 0)
         return cudaMemsetAsync(y, 0, static_cast<size_t>(M) * 4, s) == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
 
-    const int R = o.rows_per_warp;
-    const int64_t nsteps = (K + Q8::kStepElems - 1) / Q8::kStepElems;
-    if (nsteps > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
     Q8::Args a;
-    a.c = sg::make_common(M, static_cast<int>(nsteps), R, di.sm_count, Q8::kWarps);
     a.Wq = Wq; a.Wd = Wd; a.K = K; a.ldq = ldq; a.xq = xq; a.xd = xd; a.y = y;
-    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 16 / Q8::kWarps;
-    const unsigned ctas = sg::grid_ctas(a.c, static_cast<int64_t>(di.sm_count) * cps);
-    const size_t x_smem = static_cast<size_t>(nsteps) * (1024 + 64);
-    if (sg::kMaxPartials * 4 + x_smem > static_cast<size_t>(di.max_smem_optin)) return WSW_ERR_UNSUPPORTED;
-    const int lb = load_width(Wq, ldq, o.load_bytes);
-    const cudaError_t e = sg::launch_stream_gemv<Q8>(R, lb, true, a, ctas, x_smem, s, o.pdl);
-    return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
+    return q8_dense_launch<Q8>(a, M, K, o, di, s);
+}
+
+extern "C" int wsw_quantize_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, int64_t K, int64_t ldq,
+                                      const float *x, int8_t *xq_out, uint16_t *xd_out, float *y, void *stream,
+                                      const wsw_launch_opts *opts) {
+    using namespace wsw;
+    Opts o;
+    int st = resolve_opts(opts, &o);
+    if (st != WSW_OK) return st;
+    if (M < 0 || K < 0 || K % 32 != 0 || ldq % 32 != 0 || ldq < K) return WSW_ERR_INVALID_ARG;
+    if ((xq_out == nullptr) != (xd_out == nullptr)) return WSW_ERR_INVALID_ARG;
+    if (M == 0 && xq_out == nullptr) return WSW_OK;
+    if (M > 0 && !y) return WSW_ERR_INVALID_ARG;
+    if (K > 0 && (!x || (M > 0 && (!Wq || !Wd)))) return WSW_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(Wd) & 1) || (reinterpret_cast<uintptr_t>(x) & 3) ||
+        (reinterpret_cast<uintptr_t>(xd_out) & 1) || (reinterpret_cast<uintptr_t>(y) & 3))
+        return WSW_ERR_MISALIGNED;
+    if (M > (int64_t(1) << 40) || K > (int64_t(1) << 24)) return WSW_ERR_INVALID_ARG;
+    DeviceInfo di;
+    if (!device_info(&di, &st)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M == 0 || K == 0) {
+        // Nothing to multiply: the quantizer alone (an empty x needs nothing at all).
+        if (K > 0) {
+            wsw_launch_opts qo = {0, 0, o.pdl, 0};
+            const int qs = wsw_quantize_q8(x, 1, K, K, 32, xq_out, xd_out, stream, &qo);
+            if (qs != WSW_OK) return qs;
+        }
+        if (M == 0) return WSW_OK;
+        return cudaMemsetAsync(y, 0, static_cast<size_t>(M) * 4, s) == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
+    }
+    Q8X::Args a;
+    a.Wq = Wq; a.Wd = Wd; a.K = K; a.ldq = ldq; a.xq = nullptr; a.xd = nullptr; a.y = y;
+    a.x = x; a.xq_out = xq_out; a.xd_out = xd_out;
+    return q8_dense_launch<Q8X>(a, M, K, o, di, s);
 }
 
 extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E, int64_t Mo, int64_t K,

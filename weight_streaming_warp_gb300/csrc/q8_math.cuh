@@ -1,0 +1,71 @@
+// q8_math.cuh -- the per-block arithmetic of the activation quantizer, shared by the
+// standalone quantizer and the mat-vec that quantizes its own activation, so that the
+// two produce the same bytes.
+//
+// Source: "QuantizeQ8KK is thread-per-superblock: 95.5us/call ..." (vllm.cpp issue),
+// sections Cause and The donor: a per-element decomposition with a warp reduction for
+// the block scale.  A lane owns 8 consecutive values; a block of BLOCK values is
+// BLOCK / 8 adjacent lanes.
+//
+// Per block: amax = max |x|; d = amax / 127 (IEEE fp32 division);
+// q = round-half-away(x / d) (IEEE fp32 division by the fp32 d, then roundf),
+// clamped to [-127, 127]; an all-zero block has d = +0 and q = 0.
+#pragma once
+
+#include "common.cuh"
+
+namespace wsw {
+namespace q8m {
+
+// amax over the block of this lane's 8 values; every lane of the warp must call it.
+template <int BLOCK>
+__device__ __forceinline__ float block_amax(const float (&v)[8]) {
+    constexpr int LPB = BLOCK / 8;  // lanes per block
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int off = LPB / 2; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(WSW_FULL_MASK, amax, off));
+    return amax;
+}
+
+__device__ __forceinline__ float scale(float amax) { return __fdiv_rn(amax, 127.0f); }
+
+// The exact code of one value: clamp(round-half-away(fl(v / d)), -127, 127).
+__device__ __forceinline__ int code_exact(float v, float d) {
+    const float t = fminf(fmaxf(roundf(__fdiv_rn(v, d)), -127.0f), 127.0f);
+    return static_cast<int>(t);
+}
+
+// The 8 codes of this lane, packed little-endian into two words.
+//
+// Division by d is replaced by a product with r = fl(1/d), exactly.  With the
+// standard model fl(a op b) = (a op b)(1 + e), |e| <= 2^-24, and |v| <= amax so that
+// |v / d| <= 127 (1 + 2^-23): t = fl(v * r) = (v / d)(1 + e1)(1 + e2) lies within
+// |v/d| * 2.0001 * 2^-24 < 1.6e-5 of v / d, and fl(v / d) within 7.6e-6 of it, so
+// t and fl(v / d) differ by less than 2.4e-5 < 2^-15.  Rounding to the nearest
+// integer can then only differ when a half-integer lies within 2^-15 of t; for
+// those (rare) values the quotient is computed exactly.  Away from half-integers
+// round-half-even (one conversion) equals round-half-away.  A scale whose
+// reciprocal is not a normal finite number takes the exact path for every value.
+__device__ __forceinline__ void codes(const float (&v)[8], float amax, float d, uint32_t (&packed)[2]) {
+    packed[0] = packed[1] = 0u;
+    if (amax == 0.0f) return;
+    const float r = __frcp_rn(d);
+    const bool fast = d >= 1.0e-37f && d <= 1.0e37f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int q;
+        const float t = __fmul_rn(v[i], r);
+        if (fast && fabsf(t - floorf(t) - 0.5f) > 3.0517578125e-05f) {  // 2^-15 from a tie
+            q = __float2int_rn(t);
+            q = q < -127 ? -127 : (q > 127 ? 127 : q);
+        } else {
+            q = code_exact(v[i], d);
+        }
+        packed[i >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (i & 3));
+    }
+}
+
+}  // namespace q8m
+}  // namespace wsw

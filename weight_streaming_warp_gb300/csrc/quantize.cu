@@ -9,12 +9,13 @@
 // 16-byte loads, each value loaded once), a block is 4 (q8_0) or 32 (superblock)
 // adjacent lanes, and amax is reduced with warp shuffles inside that lane group.
 //
-// Per block: amax = max |x|; d = amax / 127 (IEEE fp32 division);
-// q = round-half-away(x / d) (IEEE fp32 division by the fp32 d, then roundf),
-// clamped to [-127, 127]; an all-zero block stores d = +0 and q = 0.
+// The per-block arithmetic (q8_math.cuh): amax = max |x|; d = amax / 127 (IEEE fp32
+// division); q = round-half-away(x / d) (IEEE fp32 division by the fp32 d, then
+// roundf), clamped to [-127, 127]; an all-zero block stores d = +0 and q = 0.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "q8_math.cuh"
 
 namespace wsw {
 namespace {
@@ -52,25 +53,12 @@ __global__ void __launch_bounds__(kQThreads)
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[i] = 0.0f;
         }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-#pragma unroll
-        for (int off = LPB / 2; off >= 1; off >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(WSW_FULL_MASK, amax, off));
+        const float amax = q8m::block_amax<BLOCK>(v);
         if (!active) continue;
 
-        const float d = __fdiv_rn(amax, 127.0f);
-        uint32_t packed[2] = {0u, 0u};
-        if (amax != 0.0f) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float t = roundf(__fdiv_rn(v[i], d));
-                t = fminf(fmaxf(t, -127.0f), 127.0f);
-                const uint32_t byte = static_cast<uint32_t>(static_cast<int>(t)) & 0xffu;
-                packed[i >> 2] |= byte << (8 * (i & 3));
-            }
-        }
+        const float d = q8m::scale(amax);
+        uint32_t packed[2];
+        q8m::codes(v, amax, d, packed);
         int8_t *dst = q + row * n + 8 * j;
         if (VEC) {
             *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);

@@ -277,13 +277,14 @@ inline int choose_log2_seg(int64_t M, int nsteps, int sm_count, int nw) {
 }
 
 // Host side: fill Common for M rows of `nsteps` steps, R rows per warp group and CTAs
-// of nw warps.
-inline Common make_common(int64_t M, int nsteps, int R, int sm_count, int nw) {
+// of nw warps; the K-segments follow the model for CTAs of seg_nw warps (the format's
+// own width, so that a variant with other CTAs computes the same bits).
+inline Common make_common(int64_t M, int nsteps, int R, int sm_count, int nw, int seg_nw) {
     Common c;
     c.M = M;
     c.groups = (M + R - 1) / R;
     c.nsteps = nsteps;
-    c.log2_seg = choose_log2_seg(M, nsteps, sm_count, nw);
+    c.log2_seg = choose_log2_seg(M, nsteps, sm_count, seg_nw);
     const int lw = log2_warps(nw);
     c.log2_block = c.log2_seg > lw ? c.log2_seg : lw;
     const int64_t S = int64_t(1) << c.log2_seg, B = int64_t(1) << c.log2_block;
