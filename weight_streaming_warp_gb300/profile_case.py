@@ -1,6 +1,7 @@
 """Run one hot-path call on its configured shape a few times, for a profiler.
 
     python -m weight_streaming_warp_gb300.profile_case gemv_q8_0
+    python -m weight_streaming_warp_gb300.profile_case quantize_gemv_q8_0
     python -m weight_streaming_warp_gb300.profile_case gemv_bf16 [M K]
     python -m weight_streaming_warp_gb300.profile_case gemm_bf16 [N]
     python -m weight_streaming_warp_gb300.profile_case dequant_kv [depth]
@@ -31,6 +32,15 @@ def main(argv):
         xq, xd = wsw.quantize_q8(torch.randn(K, device=dev, generator=g), 32)
         for i in range(launches):
             wsw.gemv_q8_0(Wq[i % nc], Wd[i % nc], xq, xd)
+    elif what == "quantize_gemv_q8_0":
+        M, K, nc = 14336, 4096, 4
+        Wq = [torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=g) for _ in range(nc)]
+        Wd = [(torch.rand((M, K // 32), device=dev, generator=g) * 1e-3).half() for _ in range(nc)]
+        x = torch.randn((launches, K), device=dev, generator=g)
+        xq = torch.empty(K, dtype=torch.int8, device=dev)
+        xd = torch.empty(K // 32, dtype=torch.float16, device=dev)
+        for i in range(launches):
+            wsw.quantize_gemv_q8_0(Wq[i % nc], Wd[i % nc], x[i], x_out=(xq, xd))
     elif what == "gemv_bf16":
         M, K = (int(argv[1]), int(argv[2])) if len(argv) > 2 else (5120, 17408)
         nc = max(2, (512 << 20) // (M * K * 2) + 1)
