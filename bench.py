@@ -411,25 +411,32 @@ def measure_rows(torch, wsw, dev):
         nb = depth * 4 * 128 * (1 + 2) + depth * 4 * 4 * 2
         out["dequant_kv_d%d" % depth] = {"us": round(t * 1e6, 2), "GBps": round(nb / t / 1e9, 1)}
         del qs, ds
-    # grouped MoE mat-vec (gate_up: 1536 x 2048 per expert), 128 experts, top-8
+    # grouped MoE mat-vec (gate_up: 1536 x 2048 per expert), 128 experts, top-8; calls
+    # rotate over 8 routings and 2 copies of the expert weights (2 x 403 MB), so the
+    # experts a call reads are not left in L2 by the call before
     E, Mo, Km = 128, 1536, 2048
-    Wq = torch.randint(-127, 128, (E, Mo, Km), dtype=torch.int8, device=dev, generator=g)
-    Wd = (torch.rand((E, Mo, Km // 32), device=dev, generator=g) * 1e-3).half()
+    nw, nr = 2, 8
+    Wqs = [torch.randint(-127, 128, (E, Mo, Km), dtype=torch.int8, device=dev, generator=g) for _ in range(nw)]
+    Wds = [(torch.rand((E, Mo, Km // 32), device=dev, generator=g) * 1e-3).half() for _ in range(nw)]
     for T in (1, 16, 512):
-        ids = syn.routing(0, "bench_route%d" % T, T, E, 8).to(dev)
         R = T * 8
+        idss = [syn.routing(r, "bench_route%d" % T, T, E, 8).to(dev) for r in range(nr)]
         xq = torch.randint(-127, 128, (R, Km), dtype=torch.int8, device=dev, generator=g)
         xd = torch.rand((R, Km // 32), device=dev, generator=g).half()
         y = torch.empty((R, Mo), dtype=torch.float32, device=dev)
+        it = [0]
 
-        def fn(stream, ids=ids, xq=xq, xd=xd, y=y):
-            wsw.moe_gemv_q8_0(Wq, Wd, xq, xd, ids, out=y)
+        def fn(stream, idss=idss, xq=xq, xd=xd, y=y, it=it):
+            i = it[0]
+            it[0] += 1
+            wsw.moe_gemv_q8_0(Wqs[i % nw], Wds[i % nw], xq, xd, idss[i % nr], out=y)
         t = _graph_rate(torch, fn, 8 if T == 512 else 32)
-        used = len(set(ids.tolist()))
+        used = statistics.mean(len(set(ids.tolist())) for ids in idss)
         nb = used * (Mo * Km + Mo * Km // 16) + R * (Km + Km // 16) + R * Mo * 4
         out["moe_gate_up_T%d" % T] = {"us": round(t * 1e6, 2), "experts_used": used, "GBps": round(nb / t / 1e9, 1),
-                                     "note": "weights of the used experts once + activations + y"}
-    del Wq, Wd
+                                     "note": "weights of the used experts once + activations + y; "
+                                             "8 routings x 2 weight copies rotate"}
+    del Wqs, Wds
     torch.cuda.empty_cache()
     return out
 
