@@ -388,7 +388,7 @@ extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E
         MoeTcArgs t;
         t.Wq = Wq; t.Wd = Wd; t.E = E; t.Mo = Mo; t.K = K; t.xq = xq; t.xd = xd; t.ids = ids; t.R = R;
         t.y = y; t.err = err_flag;
-        return moe_q8_tc_launch(t, s, o.pdl);
+        return moe_q8_tc_launch(t, di.sm_count, s, o.pdl);
     }
     MoeArgs a;
     a.Wq = Wq; a.Wd = Wd; a.E = E; a.Mo = Mo; a.K = K; a.xq = xq; a.xd = xd; a.ids = ids; a.R = R;

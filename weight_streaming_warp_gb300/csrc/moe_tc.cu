@@ -6,23 +6,44 @@
 // contraction (about 60 integer operations per weight byte at T = 512), so it runs on
 // tcgen05 instead of dp4a.
 //
-// Exactness.  q8_0 values are integers in [-127, 127], exact in fp16; a 32-value block
-// product sum is at most 32 * 127^2 < 2^24, exact in the fp32 accumulator.  So one
-// tcgen05.mma (kind::f16, fp16 inputs, K = 32 as two K = 16 steps) per block yields the
-// exact integer block sums for a 128-row x NT-token tile.  The epilogue scales each
-// block sum by fp32(Wd) * fp32(xd) (exact) and accumulates in fp32, blocks in order:
-//   y[m][o] = sum_b (Wd[o][b] * xd[m][b]) * isum_b(o, m).
+// Exactness.  q8_0 values are integers in [-127, 127], exact in fp16.  The weights enter
+// the MMA as they are; an activation byte q enters biased, as the binary16 value 1152 + q
+// (its bit pattern is 0x6400 | (q ^ 0x80), two byte permutes per four values).  Each
+// block sum over 32 products is then I + 1152 * S with S the block's weight sum, at most
+// 32 * 127 * 1279 < 2^23 in magnitude, so every partial sum is an integer exact in the
+// fp32 accumulator.  One B row holds the constant 1152, so the MMA also yields the
+// correction 1152 * S in its own column.  One tcgen05.mma (kind::f16, K = 32 as two K = 16
+// steps) per block gives these exact sums for 128 weight rows x up to 62 routed rows; the
+// epilogue subtracts the correction, scales by fp32(Wd) * fp32(xd) and accumulates in fp32:
+//   y[m][o] = sum_b Wd[o][b] * xd[m][b] * isum_b(o, m).
 //
-// One CTA per (expert, 128 output rows); the expert's rows are found by a stable scan of
-// the routing ids and processed in token tiles of up to 64.  Pipeline (14 warps):
-//   warp 0      TMA: raw int8 weight tiles (128 rows x 64 bytes) into a ring of 10 stages
-//   warps 1-4   convert int8 -> fp16 into 128-byte-swizzled K-major A tiles, gather the
-//               tile's activation rows (prefetched one stage ahead) into B tiles
-//   warp 5      tensor memory; one thread issues the MMAs into a ring of 8 tensor-memory
-//               slots (one 32-value block each) and commits
-//   warps 6-13  epilogue, two warpgroups, each owning 32 token columns: tcgen05.ld of the
-//               next block is in flight while the current one is scaled and accumulated;
-//               a slot is released as soon as its values are in registers
+// Persistent: one CTA per SM.  Every CTA buckets the routing ids by expert in shared
+// memory (the same stable lists in every CTA), then walks the work items i = blockIdx,
+// blockIdx + gridDim, ...; an item is (expert e, 128 output rows, up to 62 of e's routed
+// rows), items ordered by expert, then row tile, then token tile, so the grid streams
+// one contiguous window of the expert weights and the token tiles of one weight tile run
+// side by side (the second read of the tile comes from L2).  A stage is 128 K-values
+// (four blocks).  Warp roles (16 warps):
+//   warp 0       TMA: raw int8 weight tiles (128 rows x 128 bytes, 128-byte swizzle) into
+//                a ring of kRaw stages
+//   warp 1       tensor memory owner; one thread issues the MMAs: A from tensor memory,
+//                B from shared memory, D into a ring of kDPairs slots of two 64-column
+//                blocks, and commits once per pair
+//   warps 2-5    A converters: thread = weight row (its tensor-memory lane); reads its
+//                row's 128 bytes from the swizzled tile (conflict-free), converts int8 ->
+//                fp16 and writes the 64 packed columns with tcgen05.st
+//   warps 6-7    B converters: thread = B row (a routed row, or a constant row); its
+//                activation values by cp.async (one stage ahead), int8 -> biased fp16
+//                into 128-byte-swizzled K-major B tiles;
+//                halfway through an item they start the cp.async of the next item's
+//                scale rows (Wd rows as they are, padded; xd rows), and at its first stage
+//                turn the xd rows into fp32 [block][token]
+//   warps 8-15   epilogue: two groups of four warps (one per lane quarter); tcgen05.ld of
+//                a block, scale and accumulate; with at most 31 routed rows group h takes
+//                the blocks of parity h (columns 0-31) and hands its sums to group 0
+//                through shared memory, with more it takes every block for columns
+//                32 h .. 32 h + 31.  Columns 0-30 and 32-62 are routed rows, columns 31
+//                and 63 the corrections.
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -36,33 +57,49 @@ namespace {
 
 using namespace tc;
 
-constexpr int kRows = 128;     // output rows per CTA (MMA M)
-constexpr int kNTMax = 64;     // tokens per tile (MMA N <= 64)
-constexpr int kRaw = 10;       // raw weight stages (8 KB each)
-constexpr int kCvt = 3;        // converted stages (A 16 KB + B 8 KB)
-constexpr int kSlots = 8;      // tensor-memory slots (64 columns each): all 512 columns
-constexpr int kThreadsM = 448;
-constexpr int kMaxBlocks = 64;   // K <= 2048
-constexpr int kMaxList = 4096;   // rows of one expert kept in shared memory
+constexpr int kRows = 128;      // output rows per item (MMA M)
+constexpr int kCols = 64;       // B rows = accumulator columns of a block (MMA N <= 64)
+constexpr int kNT = 62;         // routed rows per item: columns 0-30 and 32-62
+constexpr int kHalf = 31;       // routed rows per 32-column half (column 31 / 63: correction)
+constexpr int kStageK = 128;    // K-values per stage (four blocks)
+constexpr int kRaw = 4;         // raw weight stages (16 KB each)
+constexpr int kAB = 2;          // A (tensor memory) and B (shared memory) slots
+constexpr int kDPairs = 3;      // accumulator slots of two blocks (64 columns each)
+constexpr int kXAhead = 2;      // activation cp.async ring (stages)
+constexpr int kMaxBlocks = 64;  // K <= 2048
+constexpr int kMaxList = 4096;  // routed rows kept in shared memory
+constexpr int kMaxE = 512;
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kBucketWarps = 8;
 
-constexpr int kXAhead = 4;     // activation stages copied ahead (cp.async ring)
-constexpr int kRawBytes = kRows * 64;
-constexpr int kABytes = kRows * 128;
-constexpr int kBBytes = kNTMax * 128;
+constexpr int kRawBytes = kRows * kStageK;       // 16 KB
+constexpr int kBAtom = kCols * 128;              // one 64-value K-major atom of B: 8 KB
+constexpr int kBBytes = 2 * kBAtom;              // 16 KB
+constexpr int kXRawBytes = kCols * kStageK;      // 8 KB
+constexpr int kScalePitch = 144;                 // bytes per staged scale row (<= 64 binary16 + pad)
+constexpr uint32_t kACol = 0;                    // A slots: columns 0 .. 127
+constexpr uint32_t kDCol = 64 * kAB;             // D slots: columns 128 .. 511 (128 per pair)
+constexpr uint32_t kTmemCols = 512;
 
 struct Smem {
-    unsigned char cvtA[kCvt][kABytes];   // 1024-aligned (first member)
-    unsigned char cvtB[kCvt][kBBytes];
-    unsigned char raw[kRaw][kRawBytes];
-    unsigned char xraw[kXAhead][kNTMax * 64];  // int8 activation rows of a stage
-    __half wscale[kRows][kMaxBlocks];
-    float xscale[kMaxBlocks][kNTMax];  // transposed: one block's token scales are contiguous
-    int list[kMaxList];
+    unsigned char raw[kRaw][kRawBytes];     // 1024-aligned (first member); bucketing scratch first
+    unsigned char bt[kAB][kBBytes];         // 1024-aligned
+    unsigned char xraw[kXAhead][kXRawBytes];  // row t: 16-byte chunk j at (j ^ (t & 7))
+    unsigned char wd[2][kRows * kScalePitch];  // per item (double-buffered): Wd rows, padded
+    unsigned char xdr[kCols * kScalePitch];   // the next item's xd rows, padded
+    float xs[2][kMaxBlocks][kCols];           // per item: xd as fp32, [block][column]
+    float comb[32][kRows];                    // group 1 -> group 0 partial sums (<= 32 rows)
+    uint16_t list[kMaxList];
+    int cnt[kMaxE];
+    int off[kMaxE];
+    int ibase[kMaxE + 1];
     uint64_t raw_full[kRaw], raw_empty[kRaw];
-    uint64_t cvt_full[kCvt], cvt_empty[kCvt];
-    uint64_t slot_full[kSlots], slot_empty[kSlots];
+    uint64_t a_full[kAB], b_full[kAB], ab_empty[kAB];
+    uint64_t d_full[kDPairs], d_empty[kDPairs];
+    uint64_t s_full[2], s_empty[2];
     uint32_t tmem_slot;
-    int count;
+    int nitems;
 };
 
 // byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled K-major tile
@@ -74,7 +111,7 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c) {
 // sign bit flipped is u = q + 128; the binary16 pattern 0x6400 | u is 1024 + u, and
 // subtracting 1152 (0x6480) leaves q exactly.  Two byte permutes and two half2
 // subtractions per four values.
-__device__ __forceinline__ void i8x16_to_h(const uint4 &v, uint32_t (&o)[8]) {
+__device__ __forceinline__ void i8x16_to_h(const uint4 &v, uint32_t *o) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
 #pragma unroll
@@ -89,64 +126,182 @@ __device__ __forceinline__ void i8x16_to_h(const uint4 &v, uint32_t (&o)[8]) {
     }
 }
 
-__global__ void __launch_bounds__(kThreadsM, 1)
-    moe_q8_tc_kernel(const __grid_constant__ CUtensorMap tmWq, const MoeTcArgs a, int m_tiles) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
+        "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// D = A (tensor memory) x B (shared memory descriptor), kind::f16.
+__device__ __forceinline__ void mma_ts(uint32_t dtmem, uint32_t atmem, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(dtmem),
+        "r"(atmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// One work item of this CTA.
+struct Item {
+    int e;     // expert
+    int m0;    // first output row
+    int tok0;  // first routed row in the expert-ordered list
+    int n;     // routed rows (1 .. kNT)
+};
+
+__device__ __forceinline__ void decode_item(const Smem &S, int i, int &ecur, Item &it) {
+    while (S.ibase[ecur + 1] <= i) ++ecur;
+    const int c = S.cnt[ecur];
+    const int ntt = (c + kNT - 1) / kNT;
+    const int local = i - S.ibase[ecur];
+    const int mt = local / ntt, tt = local - mt * ntt;
+    it.e = ecur;
+    it.m0 = mt * kRows;
+    it.tok0 = S.off[ecur] + tt * kNT;
+    it.n = c - tt * kNT < kNT ? c - tt * kNT : kNT;
+}
+
+// accumulator column of routed row t of an item, and back (-1: a correction column)
+__device__ __forceinline__ int col_of(int t) { return t < kHalf ? t : t + 1; }
+__device__ __forceinline__ int tok_of(int col) { return (col & 31) == kHalf ? -1 : (col < 32 ? col : col - 1); }
+// MMA N of an item with n routed rows: one half (and its correction) or both
+__device__ __forceinline__ int cols_of(int n) { return n <= kHalf ? 32 : 64; }
+
+// 16 int8 values -> 16 biased binary16 values 1152 + q (exact), as 8 packed half2 words
+__device__ __forceinline__ void i8x16_to_h_biased(const uint4 &v, uint32_t *o) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t u = w[i] ^ 0x80808080u;
+        o[2 * i] = __byte_perm(u, 0x64646464u, 0x4140);      // 1024 + u0, 1024 + u1
+        o[2 * i + 1] = __byte_perm(u, 0x64646464u, 0x4342);  // 1024 + u2, 1024 + u3
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_q8_tc_kernel(const __grid_constant__ CUtensorMap tmWq, const MoeTcArgs a) {
     extern __shared__ unsigned char smem_raw[];
     Smem &S = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t e = blockIdx.x / m_tiles;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.x % m_tiles) * kRows;
-    const int nb = static_cast<int>(a.K / 32);  // 32-value blocks per row
-    const int kst = nb / 2 + (nb & 1);          // 64-value stages per token tile
+    const int E = static_cast<int>(a.E);
+    const int R = static_cast<int>(a.R);
+    const int nb = static_cast<int>(a.K / 32);       // blocks per row
+    const int kst = static_cast<int>(a.K / kStageK); // stages per item
+    const int m_tiles = static_cast<int>((a.Mo + kRows - 1) / kRows);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRaw; ++i) { mbar_init(&S.raw_full[i], 1); mbar_init(&S.raw_empty[i], 128); }
+        for (int i = 0; i < kAB; ++i) {
+            mbar_init(&S.a_full[i], 128); mbar_init(&S.b_full[i], 64); mbar_init(&S.ab_empty[i], 1);
+        }
+        for (int i = 0; i < kDPairs; ++i) { mbar_init(&S.d_full[i], 1); mbar_init(&S.d_empty[i], 8); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&S.s_full[i], 64); mbar_init(&S.s_empty[i], 256); }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
 
     pdl_wait();  // ids and activations come from earlier kernels
-    if (blockIdx.x == 0 && a.err) {
-        for (int64_t m = threadIdx.x; m < a.R; m += kThreadsM) {
+
+    // ------------------------------------------------------------ bucketing
+    // Stable per-expert lists of the routed rows (every CTA builds the same ones).
+    int *ids_s = reinterpret_cast<int *>(&S.raw[0][0]);
+    int *wcnt = ids_s + R;  // [kBucketWarps][E]
+    {
+        bool bad = false;
+        for (int m = threadIdx.x; m < R; m += kThreads) {
             const int id = a.ids[m];
-            if (id < 0 || id >= a.E) atomicOr(a.err, 1);
+            const bool ok = id >= 0 && id < E;
+            ids_s[m] = ok ? id : -1;
+            bad |= !ok;
         }
+        if (bad && blockIdx.x == 0 && a.err) atomicOr(a.err, 1);
+        for (int i = threadIdx.x; i < kBucketWarps * E; i += kThreads) wcnt[i] = 0;
     }
-    // Routing ids into shared memory (coalesced, all threads; the converted-tile ring
-    // is free until the main loop), then a stable list of this expert's rows.
-    int *ids_s = reinterpret_cast<int *>(S.cvtA[0]);  // room for kCvt * kABytes / 4 ids
-    if ((reinterpret_cast<uintptr_t>(a.ids) & 15) == 0) {
-        const int64_t n4 = a.R / 4;
-        for (int64_t i = threadIdx.x; i < n4; i += kThreadsM)
-            reinterpret_cast<int4 *>(ids_s)[i] = __ldg(reinterpret_cast<const int4 *>(a.ids) + i);
-        for (int64_t m = 4 * n4 + threadIdx.x; m < a.R; m += kThreadsM) ids_s[m] = a.ids[m];
-    } else {
-        for (int64_t m = threadIdx.x; m < a.R; m += kThreadsM) ids_s[m] = a.ids[m];
+    __syncthreads();
+    const int r0 = warp < kBucketWarps ? static_cast<int>(static_cast<int64_t>(warp) * R / kBucketWarps) : 0;
+    const int r1 = warp < kBucketWarps ? static_cast<int>(static_cast<int64_t>(warp + 1) * R / kBucketWarps) : 0;
+    for (int base = r0; base < r1; base += 32) {
+        const int m = base + lane;
+        const int e = m < r1 ? ids_s[m] : -1;
+        const unsigned peers = __match_any_sync(WSW_FULL_MASK, e >= 0 ? e : E + lane);
+        if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < kBucketWarps; ++w) {
+            const int c = wcnt[w * E + e];
+            wcnt[w * E + e] = run;
+            run += c;
+        }
+        S.cnt[e] = run;
     }
     __syncthreads();
     if (warp == 0) {
-        int n = 0;
-        for (int64_t base = 0; base < a.R; base += 32) {
-            const int64_t m = base + lane;
-            const bool hit = m < a.R && ids_s[m] == static_cast<int>(e);
-            const unsigned bal = __ballot_sync(WSW_FULL_MASK, hit);
-            if (hit) {
-                const int pos = n + __popc(bal & ((1u << lane) - 1u));
-                if (pos < kMaxList) S.list[pos] = static_cast<int>(m);
+        // exclusive scans over the experts: list offsets and item bases
+        int run = 0, irun = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int c = e < E ? S.cnt[e] : 0;
+            const int items = m_tiles * ((c + kNT - 1) / kNT);
+            int incl = c, iincl = items;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(WSW_FULL_MASK, incl, o);
+                const int it = __shfl_up_sync(WSW_FULL_MASK, iincl, o);
+                if (lane >= o) { incl += t; iincl += it; }
             }
-            n += __popc(bal);
+            if (e < E) {
+                S.off[e] = run + incl - c;
+                S.ibase[e] = irun + iincl - items;
+            }
+            run += __shfl_sync(WSW_FULL_MASK, incl, 31);
+            irun += __shfl_sync(WSW_FULL_MASK, iincl, 31);
         }
-        if (lane == 0) S.count = n < kMaxList ? n : kMaxList;
-    }
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kRaw; ++i) { mbar_init(&S.raw_full[i], 1); mbar_init(&S.raw_empty[i], 128); }
-        for (int i = 0; i < kCvt; ++i) { mbar_init(&S.cvt_full[i], 128); mbar_init(&S.cvt_empty[i], 1); }
-        for (int i = 0; i < kSlots; ++i) { mbar_init(&S.slot_full[i], 1); mbar_init(&S.slot_empty[i], 256); }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (lane == 0) {
+            S.ibase[E] = irun;
+            S.nitems = irun;
+        }
     }
     __syncthreads();
-    const int n_e = S.count;
+    for (int base = r0; base < r1; base += 32) {
+        const int m = base + lane;
+        const int e = m < r1 ? ids_s[m] : -1;
+        const unsigned peers = __match_any_sync(WSW_FULL_MASK, e >= 0 ? e : E + lane);
+        if (e >= 0) S.list[S.off[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u))] = static_cast<uint16_t>(m);
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();  // the raw ring is free again
     pdl_launch_dependents();
-    if (n_e == 0) return;  // expert unused: no tensor memory was taken
+    const int NI = S.nitems;
+    const int C = static_cast<int>(gridDim.x);
+    if (static_cast<int>(blockIdx.x) >= NI) return;  // no items: no tensor memory was taken
+    const int my_items = (NI - 1 - static_cast<int>(blockIdx.x)) / C + 1;
 
-    if (warp == 5) {
+    if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&S.tmem_slot)),
-                     "r"(kSlots * kNTMax)
+                     "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -154,230 +309,318 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = S.tmem_slot;
-    const int tiles = (n_e + kNTMax - 1) / kNTMax;
-    const int total = tiles * kst;  // stages over all token tiles
     bool ok = true;
+    int ecur = 0;
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmWq)) : "memory");
-            uint64_t pol;
-            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-            for (int i = 0; i < total && ok; ++i) {
-                const int r = i % kRaw;
-                if (!mbar_wait(&S.raw_empty[r], ((i / kRaw) & 1u) ^ 1u)) { ok = false; break; }
-                mbar_expect_tx(&S.raw_full[r], kRawBytes);
-                tma_load_2d(S.raw[r], &tmWq, (i % kst) * 64, static_cast<int>(e * a.Mo + m0), &S.raw_full[r], pol);
+            uint64_t pol_first, pol_last;
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_first));
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_last));
+            for (int k = 0; k < my_items && ok; ++k) {
+                Item it;
+                decode_item(S, static_cast<int>(blockIdx.x) + k * C, ecur, it);
+                // the tile is read again by the expert's next token tile unless this is its last
+                const bool last_tt = it.tok0 + it.n >= S.off[it.e] + S.cnt[it.e];
+                const uint64_t pol = last_tt ? pol_first : pol_last;
+                const int y = static_cast<int>(it.e * a.Mo + it.m0);
+                for (int s = 0; s < kst; ++s) {
+                    const int g = k * kst + s, r = g % kRaw;
+                    if (!mbar_wait(&S.raw_empty[r], ((g / kRaw) & 1u) ^ 1u)) { ok = false; break; }
+                    mbar_expect_tx(&S.raw_full[r], kRawBytes);
+                    tma_load_2d(S.raw[r], &tmWq, s * kStageK, y, &S.raw_full[r], pol);
+                }
             }
         }
         __syncwarp();
-    } else if (warp >= 1 && warp <= 4) {
-        // ---------------------------------------------------------- converters
-        const int c = threadIdx.x - 32;  // 0..127
-        const int ch = c & 3;            // 16-byte chunk of a 64-byte raw row
-        const int tt = c >> 1, hf = c & 1;  // B: token row, half of the 64 values
-        // activation rows of stage i -> xraw[i % kXAhead], 32 bytes per thread, copied
-        // kXAhead - 1 stages ahead; rows past the expert's count are zero-filled
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            for (int k = 0; k < my_items && ok; ++k) {
+                Item it;
+                decode_item(S, static_cast<int>(blockIdx.x) + k * C, ecur, it);
+                const uint32_t idesc = instr_desc(kRows, cols_of(it.n), false);
+                for (int s = 0; s < kst && ok; ++s) {
+                    const int g = k * kst + s, v = g % kAB;
+                    const uint32_t ph = (g / kAB) & 1u;
+                    if (!mbar_wait(&S.a_full[v], ph) || !mbar_wait(&S.b_full[v], ph)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t bd = sw128_desc(saddr(S.bt[v]));
+                    for (int pp = 0; pp < 2; ++pp) {
+                        const int gp = 2 * g + pp, p = gp % kDPairs;
+                        if (!mbar_wait(&S.d_empty[p], ((gp / kDPairs) & 1u) ^ 1u)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int j = 2 * pp + jj;  // block of the stage
+                            const uint32_t d = tmem + kDCol + static_cast<uint32_t>(128 * p + 64 * jj);
+                            const uint32_t at = tmem + kACol + static_cast<uint32_t>(64 * v + 16 * j);
+                            // block j: atom j / 2 of the B tile, bytes 64 (j % 2) + {0, 32} of its rows
+                            const uint64_t b0 = bd + static_cast<uint64_t>((j >> 1) * (kBAtom >> 4) + (j & 1) * 4);
+                            mma_ts(d, at, b0, idesc, 0u);
+                            mma_ts(d, at + 8, b0 + 2, idesc, 1u);
+                        }
+                        mma_commit(&S.d_full[p]);
+                    }
+                    mma_commit(&S.ab_empty[v]);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp <= 5) {
+        // ---------------------------------------------------------- A converters
+        const int qd = warp & 3;
+        const int row = 32 * qd + lane;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * qd) << 16) + kACol;
+        for (int k = 0; k < my_items && ok; ++k) {
+            for (int s = 0; s < kst; ++s) {
+                const int g = k * kst + s, r = g % kRaw, v = g % kAB;
+                if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.raw_full[r], (g / kRaw) & 1u))) { ok = false; break; }
+                uint4 raw[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4 *>(S.raw[r] + sw_off(row, c));
+                if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.ab_empty[v], ((g / kAB) & 1u) ^ 1u))) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) i8x16_to_h(raw[4 * h + c], &w[8 * c]);
+                    tmem_st32(lane_addr + static_cast<uint32_t>(64 * v + 32 * h), w);
+                }
+                // The raw slot goes back to the TMA (async proxy) only after its values have
+                // been consumed, with a proxy fence between the reads and the refill.
+                fence_async_shared();
+                mbar_arrive(&S.raw_empty[r]);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                mbar_arrive(&S.a_full[v]);
+            }
+        }
+    } else if (warp <= 7) {
+        // ---------------------------------------------------------- B converters
+        const int tt = threadIdx.x - 6 * 32;  // 0..63: B row = accumulator column
+        const int tk = tok_of(tt);            // routed row of the item in this column, or -1
+        // The correction rows (constant 1152) are written once into both B slots.
+        if (tk < 0) {
+            const uint32_t c1152 = 0x64806480u;
+#pragma unroll
+            for (int v = 0; v < kAB; ++v)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<uint4 *>(S.bt[v] + h * kBAtom + sw_off(tt, i)) =
+                            make_uint4(c1152, c1152, c1152, c1152);
+            fence_async_shared();
+        }
+        const int total = my_items * kst;
+        const int pieces = nb / 8;            // 16-byte pieces of a scale row
+        int kc = -1;  // item whose token row `xrow` describes
+        Item cit;
+        int ec2 = 0, ec3 = 0;
+        const int8_t *xrow = nullptr;
+        bool xzero = false;  // row inside the MMA's N but past the routed rows: zeros
+        // the 128 activation values of token tt for global stage i -> xraw[i % kXAhead]
         auto copy_x = [&](int i) {
             if (i < total) {
-                const int tile = i / kst, ks = i % kst;
-                const int t = tile * kNTMax + tt;
-                const bool valid = t < n_e;
-                const int8_t *src = valid ? a.xq + static_cast<int64_t>(S.list[t]) * a.K + ks * 64 + hf * 32 : a.xq;
-                const uint32_t dst = saddr(S.xraw[i % kXAhead] + tt * 64 + hf * 32);
-                const uint32_t n = valid ? 16u : 0u;
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + 16), "l"(src + 16), "r"(n)
-                             : "memory");
+                const int k = i / kst, s = i - k * kst;
+                if (k != kc) {
+                    decode_item(S, static_cast<int>(blockIdx.x) + k * C, ec2, cit);
+                    kc = k;
+                    xrow = tk >= 0 && tk < cit.n ? a.xq + static_cast<int64_t>(S.list[cit.tok0 + tk]) * a.K : nullptr;
+                    xzero = tk >= cit.n && tt < cols_of(cit.n);
+                }
+                if (xrow || xzero) {
+                    const int8_t *src = xrow ? xrow + s * kStageK : a.xq;
+                    const uint32_t n = xrow ? 16u : 0u;
+                    const uint32_t dst = saddr(S.xraw[i % kXAhead] + tt * kStageK);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + ((j ^ (tt & 7)) << 4)),
+                                     "l"(src + 16 * j), "r"(n)
+                                     : "memory");
+                }
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
-        for (int i = 0; i < kXAhead - 1; ++i) copy_x(i);
-        for (int i = 0; i < total && ok; ++i) {
-            const int r = i % kRaw, v = i % kCvt;
-            copy_x(i + kXAhead - 1);
-            if (!mbar_wait(&S.raw_full[r], (i / kRaw) & 1u)) { ok = false; break; }
-            if (!mbar_wait(&S.cvt_empty[v], ((i / kCvt) & 1u) ^ 1u)) { ok = false; break; }
-            unsigned char *A = S.cvtA[v];
+        // the scale rows of item kk (128 Wd rows into wd[kk % 2], this thread's xd row into
+        // xdr) join the cp.async group committed next; buffer kk % 2 must be released by
+        // the epilogue of item kk - 2 first
+        auto copy_scales = [&](int kk) -> bool {
+            if (kk >= my_items) return true;
+            Item si;
+            decode_item(S, static_cast<int>(blockIdx.x) + kk * C, ec3, si);
+            if (!mbar_wait(&S.s_empty[kk & 1], ((kk >> 1) & 1u) ^ 1u)) return false;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int row = (c >> 2) + 32 * j;
-                const uint4 raw = *reinterpret_cast<const uint4 *>(S.raw[r] + row * 64 + ch * 16);
-                uint32_t h[8];
-                i8x16_to_h(raw, h);
-                *reinterpret_cast<uint4 *>(A + sw_off(row, 2 * ch)) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4 *>(A + sw_off(row, 2 * ch + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = tt + 64 * rr;
+                const int64_t o = si.m0 + r;
+                const bool valid = o < a.Mo;
+                const uint16_t *src = a.Wd + (si.e * a.Mo + (valid ? o : 0)) * nb;
+                const uint32_t dst = saddr(S.wd[kk & 1] + r * kScalePitch);
+                for (int p = 0; p < pieces; ++p)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + 16 * p), "l"(src + 8 * p),
+                                 "r"(valid ? 16u : 0u)
+                                 : "memory");
             }
-            mbar_arrive(&S.raw_empty[r]);
-            // this stage's activation copy has landed (kXAhead - 1 newer groups may pend)
-            asm volatile("cp.async.wait_group %0;" ::"n"(kXAhead - 1) : "memory");
-            const uint4 x0 = *reinterpret_cast<const uint4 *>(S.xraw[i % kXAhead] + tt * 64 + hf * 32);
-            const uint4 x1 = *reinterpret_cast<const uint4 *>(S.xraw[i % kXAhead] + tt * 64 + hf * 32 + 16);
-            unsigned char *B = S.cvtB[v];
-            uint32_t h0[8], h1[8];
-            i8x16_to_h(x0, h0);
-            i8x16_to_h(x1, h1);
-            *reinterpret_cast<uint4 *>(B + sw_off(tt, 4 * hf)) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
-            *reinterpret_cast<uint4 *>(B + sw_off(tt, 4 * hf + 1)) = make_uint4(h0[4], h0[5], h0[6], h0[7]);
-            *reinterpret_cast<uint4 *>(B + sw_off(tt, 4 * hf + 2)) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-            *reinterpret_cast<uint4 *>(B + sw_off(tt, 4 * hf + 3)) = make_uint4(h1[4], h1[5], h1[6], h1[7]);
-            fence_async_shared();
-            mbar_arrive(&S.cvt_full[v]);
+            const bool valid = tk >= 0 && tk < si.n;
+            const uint16_t *src = a.xd + static_cast<int64_t>(valid ? S.list[si.tok0 + tk] : 0) * nb;
+            const uint32_t dst = saddr(S.xdr + tt * kScalePitch);
+            for (int p = 0; p < pieces; ++p)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + 16 * p), "l"(src + 8 * p),
+                             "r"(valid ? 16u : 0u)
+                             : "memory");
+            return true;
+        };
+        if (!copy_scales(0)) ok = false;
+        for (int i = 0; i < kXAhead - 1; ++i) copy_x(i);
+        for (int k = 0; k < my_items && ok; ++k) {
+            Item it;
+            decode_item(S, static_cast<int>(blockIdx.x) + k * C, ecur, it);
+            const int N = cols_of(it.n);
+            for (int s = 0; s < kst; ++s) {
+                const int g = k * kst + s, v = g % kAB;
+                if (s == kst / 2 && !copy_scales(k + 1)) { ok = false; break; }
+                copy_x(g + kXAhead - 1);
+                asm volatile("cp.async.wait_group %0;" ::"n"(kXAhead - 1) : "memory");
+                if (s == 0) {
+                    // this item's scale rows have landed: xd -> fp32 [block][token]
+                    const unsigned char *xr = S.xdr + tt * kScalePitch;
+                    for (int p = 0; p < pieces; ++p) {
+                        const uint4 v4 = *reinterpret_cast<const uint4 *>(xr + 16 * p);
+                        const __half *h = reinterpret_cast<const __half *>(&v4);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) S.xs[k & 1][8 * p + i][tt] = __half2float(h[i]);
+                    }
+                    mbar_arrive(&S.s_full[k & 1]);
+                }
+                const unsigned char *xr = S.xraw[g % kXAhead] + tt * kStageK;
+                if (!mbar_wait(&S.ab_empty[v], ((g / kAB) & 1u) ^ 1u)) { ok = false; break; }
+                if (tt < N && tk >= 0) {
+                    // values 64 h .. 64 h + 63 of the stage = atom h of the B tile
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            i8x16_to_h_biased(*reinterpret_cast<const uint4 *>(xr + (((4 * h + j) ^ (tt & 7)) << 4)), &w[8 * j]);
+                        unsigned char *B = S.bt[v] + h * kBAtom;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            *reinterpret_cast<uint4 *>(B + sw_off(tt, i)) =
+                                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
+                    fence_async_shared();
+                }
+                mbar_arrive(&S.b_full[v]);
+            }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == 5) {
-        // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            int g = 0;  // block counter over all tiles
-            for (int i = 0; i < total && ok; ++i) {
-                const int v = i % kCvt;
-                const int tile = i / kst, ks = i % kst;
-                const int nt_tok = n_e - tile * kNTMax < kNTMax ? n_e - tile * kNTMax : kNTMax;
-                const int NT = (nt_tok + 15) & ~15;
-                const uint32_t idesc = instr_desc(kRows, NT, false);
-                if (!mbar_wait(&S.cvt_full[v], (i / kCvt) & 1u)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t dA = sw128_desc(saddr(S.cvtA[v]));
-                const uint64_t dB = sw128_desc(saddr(S.cvtB[v]));
-                const int nblk_here = (2 * ks + 1 < nb) ? 2 : 1;
-                for (int j = 0; j < nblk_here; ++j, ++g) {
-                    const int q = g % kSlots;
-                    if (!mbar_wait(&S.slot_empty[q], ((g / kSlots) & 1u) ^ 1u)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d = tmem + static_cast<uint32_t>(q * kNTMax);
-                    mma_bf16(d, dA + 4 * j, dB + 4 * j, idesc, 0u);          // values 32j .. 32j+15
-                    mma_bf16(d, dA + 4 * j + 2, dB + 4 * j + 2, idesc, 1u);  // values 32j+16 .. 32j+31
-                    mma_commit(&S.slot_full[q]);
-                }
-                mma_commit(&S.cvt_empty[v]);
-            }
-        }
-        __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue
+        // Two groups of four warps (one per lane quarter).  Items with at most 32 routed
+        // rows: group h takes the blocks of parity h (32 columns each) and group 1 hands
+        // its sums to group 0; items with more: group h takes every block, columns
+        // 32 h .. 32 h + 31.
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
-        const int wg = (warp - 6) >> 2;  // token columns 32*wg .. 32*wg+31
-        const int64_t o = m0 + row;
-        const int et = threadIdx.x - 192;  // 0..255 among the epilogue threads
-        // this CTA's weight scales: each row's nb values are 2*nb contiguous bytes;
-        // warpgroup wg loads 16-byte pieces wg, wg+2, ... (all issued before use)
-        if (o < a.Mo) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.Wd + (e * a.Mo + o) * nb);
-            uint4 v[kMaxBlocks / 16];
+        const int grp = (warp - 8) >> 2;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * qd) << 16) + kDCol;
+        for (int k = 0; k < my_items; ++k) {
+            Item it;
+            decode_item(S, static_cast<int>(blockIdx.x) + k * C, ecur, it);
+            const int sb = k & 1;
+            const bool split_cols = it.n > kHalf;
+            const int c0 = split_cols ? 32 * grp : 0;  // first accumulator column of this thread
+            if (ok && !__all_sync(WSW_FULL_MASK, mbar_wait(&S.s_full[sb], (k >> 1) & 1u))) ok = false;
+            float acc[kHalf];
 #pragma unroll
-            for (int j = 0; j < kMaxBlocks / 16; ++j)
-                if (8 * (2 * j + wg) < nb) v[j] = __ldg(src + 2 * j + wg);
-#pragma unroll
-            for (int j = 0; j < kMaxBlocks / 16; ++j)
-                if (8 * (2 * j + wg) < nb) *reinterpret_cast<uint4 *>(&S.wscale[row][8 * (2 * j + wg)]) = v[j];
-        }
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16) + static_cast<uint32_t>(32 * wg);
-        int g = 0;
-        for (int tile = 0; tile < tiles; ++tile) {
-            const int nt_tok = n_e - tile * kNTMax < kNTMax ? n_e - tile * kNTMax : kNTMax;
-            const bool mine = 32 * wg < nt_tok;  // this warpgroup has token columns in the tile
-            // the tile's activation scales, fp32, transposed (named barrier 1: 256 threads)
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            {
-                // token t's nb scales are 2*nb contiguous bytes: 16-byte pieces, two per thread
-                constexpr int kPieces = kNTMax * kMaxBlocks / 8;  // 512 >= kNTMax * nb / 8
-                uint4 v[kPieces / 256];
-                int tk[kPieces / 256], pc[kPieces / 256];
-#pragma unroll
-                for (int j = 0; j < kPieces / 256; ++j) {
-                    const int idx = et + 256 * j;
-                    tk[j] = idx / (nb / 8);
-                    pc[j] = idx % (nb / 8);
-                    v[j] = make_uint4(0u, 0u, 0u, 0u);
-                    if (tk[j] < nt_tok)
-                        v[j] = __ldg(reinterpret_cast<const uint4 *>(
-                                         a.xd + static_cast<int64_t>(S.list[tile * kNTMax + tk[j]]) * nb) + pc[j]);
-                }
-#pragma unroll
-                for (int j = 0; j < kPieces / 256; ++j) {
-                    if (tk[j] < kNTMax) {
-                        const __half *h = reinterpret_cast<const __half *>(&v[j]);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) S.xscale[8 * pc[j] + i][tk[j]] = __half2float(h[i]);
-                    }
-                }
-            }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            float acc[32];
-#pragma unroll
-            for (int t = 0; t < 32; ++t) acc[t] = 0.0f;
-            float va[32], vb[32];
-            // block b of this tile lives in slot (g + b) % kSlots
-            auto fetch = [&](int b, float(&v)[32]) -> bool {
-                const int gg = g + b, q = gg % kSlots;
-                if (!ok || !mbar_wait(&S.slot_full[q], (gg / kSlots) & 1u)) { ok = false; return false; }
-                tc_fence_after();
-                if (mine) {
-                    uint32_t r[32];
-                    asm volatile(
-                        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-                          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-                          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-                          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-                        : "r"(lane_base + static_cast<uint32_t>(q * kNTMax)));
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                }
-                return true;
-            };
-            auto release = [&](int b) {
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                tc_fence_before();
-                mbar_arrive(&S.slot_empty[(g + b) % kSlots]);
-            };
-            auto scale_add = [&](int b, const float(&v)[32]) {
-                if (!mine) return;
-                const float wd = __half2float(S.wscale[row][b]);
-                const float4 *xs4 = reinterpret_cast<const float4 *>(&S.xscale[b][32 * wg]);
+            for (int j = 0; j < kHalf; ++j) acc[j] = 0.0f;
+            // block b's 32 columns c0 .. c0 + 31: routed rows, then the correction 1152 * S
+            auto scale_add = [&](int b, const uint32_t(&dv)[32]) {
+                const float wd = __half2float(reinterpret_cast<const __half *>(S.wd[sb] + row * kScalePitch)[b]);
+                const float wdc = wd * __uint_as_float(dv[kHalf]);
+                const float4 *xs4 = reinterpret_cast<const float4 *>(&S.xs[sb][b][c0]);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 xs = xs4[j4];
-                    acc[4 * j4 + 0] = fmaf(wd * xs.x, v[4 * j4 + 0], acc[4 * j4 + 0]);
-                    acc[4 * j4 + 1] = fmaf(wd * xs.y, v[4 * j4 + 1], acc[4 * j4 + 1]);
-                    acc[4 * j4 + 2] = fmaf(wd * xs.z, v[4 * j4 + 2], acc[4 * j4 + 2]);
-                    acc[4 * j4 + 3] = fmaf(wd * xs.w, v[4 * j4 + 3], acc[4 * j4 + 3]);
+                    const float x[4] = {xs.x, xs.y, xs.z, xs.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int j = 4 * j4 + i;
+                        if (j < kHalf)  // Wd * isum = Wd * (D - 1152 S), one rounding
+                            acc[j] = fmaf(x[i], fmaf(__uint_as_float(dv[j]), wd, -wdc), acc[j]);
+                    }
                 }
             };
-            bool have = fetch(0, va);
-            if (have) release(0);
-            for (int b = 0; b < nb; b += 2) {
-                // va holds block b; vb receives block b+1 while b is scaled
-                const bool hb = (b + 1 < nb) && fetch(b + 1, vb);
-                if (have) scale_add(b, va);
-                if (hb) release(b + 1);
-                const bool ha = (b + 2 < nb) && fetch(b + 2, va);
-                if (hb) scale_add(b + 1, vb);
-                if (ha) release(b + 2);
-                have = ha;
-            }
-            g += nb;
-            if (o < a.Mo && mine) {
-#pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    const int tt = 32 * wg + t;
-                    if (tt < nt_tok)
-                        a.y[static_cast<int64_t>(S.list[tile * kNTMax + tt]) * a.Mo + o] =
-                            ok ? acc[t] : __int_as_float(0x7fc00000);
+            // pair gp = 2 g + pp holds blocks 4 s + 2 pp and 4 s + 2 pp + 1 of stage s
+            for (int s = 0; s < kst && ok; ++s) {
+                for (int pp = 0; pp < 2 && ok; ++pp) {
+                    const int gp = 2 * (k * kst + s) + pp, p = gp % kDPairs;
+                    if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.d_full[p], (gp / kDPairs) & 1u))) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t pa = lane_addr + static_cast<uint32_t>(128 * p);
+                    uint32_t dv[32];
+                    if (!split_cols) {
+                        tmem_ld32(pa + static_cast<uint32_t>(64 * grp), dv);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&S.d_empty[p]);
+                        scale_add(4 * s + 2 * pp + grp, dv);
+                    } else {
+                        tmem_ld32(pa + static_cast<uint32_t>(c0), dv);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        scale_add(4 * s + 2 * pp, dv);
+                        tmem_ld32(pa + static_cast<uint32_t>(64 + c0), dv);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&S.d_empty[p]);
+                        scale_add(4 * s + 2 * pp + 1, dv);
+                    }
                 }
+            }
+            mbar_arrive(&S.s_empty[sb]);
+            const int64_t o = it.m0 + row;
+            const float nan = __int_as_float(0x7fc00000);
+            if (split_cols) {
+                const int t0 = grp * kHalf;  // routed rows of columns c0 .. c0 + 30
+                if (o < a.Mo) {
+#pragma unroll
+                    for (int j = 0; j < kHalf; ++j)
+                        if (t0 + j < it.n)
+                            a.y[static_cast<int64_t>(S.list[it.tok0 + t0 + j]) * a.Mo + o] = ok ? acc[j] : nan;
+                }
+            } else {
+                // group 1 hands its sums to group 0
+                if (grp == 1) {
+#pragma unroll
+                    for (int j = 0; j < kHalf; ++j) S.comb[j][row] = ok ? acc[j] : nan;
+                }
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                if (grp == 0 && o < a.Mo) {
+#pragma unroll
+                    for (int j = 0; j < kHalf; ++j)
+                        if (j < it.n)
+                            a.y[static_cast<int64_t>(S.list[it.tok0 + j]) * a.Mo + o] =
+                                ok ? acc[j] + S.comb[j][row] : nan;
+                }
+                asm volatile("bar.sync 1, 256;" ::: "memory");
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kSlots * kNTMax)
-                     : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
 }
 
@@ -400,32 +643,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_moe() {
 // Whether the tensor-core path takes this problem (the caller falls back otherwise).
 bool moe_q8_tc_supported(int64_t E, int64_t Mo, int64_t K, int64_t R, const void *Wq, const void *Wd,
                          const void *xq, const void *xd) {
-    // K: whole 64-value stages, at most kMaxBlocks blocks; the scale rows (2 * K/32
-    // bytes) split into 16-byte pieces; the routing ids fit the staging area.
-    return K % 256 == 0 && K / 32 <= kMaxBlocks && R <= kMaxList && R * 4 <= kCvt * kABytes &&
-           E * Mo <= 0x7fffffffLL &&
+    // K: whole 128-value stages and 16-byte pieces of a scale row (K % 256), at most
+    // kMaxBlocks blocks; the routing ids and per-warp counts fit the raw ring during
+    // bucketing; the lists fit shared memory.
+    return K % 256 == 0 && K / 32 <= kMaxBlocks && R <= kMaxList && E <= kMaxE &&
+           (R + kBucketWarps * E) * 4 <= kRaw * kRawBytes && E * Mo <= 0x7fffffffLL &&
            ((reinterpret_cast<uintptr_t>(Wq) | reinterpret_cast<uintptr_t>(Wd) | reinterpret_cast<uintptr_t>(xq) |
              reinterpret_cast<uintptr_t>(xd)) & 15) == 0;
 }
 
-int moe_q8_tc_launch(const MoeTcArgs &a, cudaStream_t s, bool pdl) {
+int moe_q8_tc_launch(const MoeTcArgs &a, int sm_count, cudaStream_t s, bool pdl) {
     auto fn = encode_fn_moe();
     if (!fn) return WSW_ERR_CUDA;
     CUtensorMap map;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.E * a.Mo)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K)};
-    cuuint32_t box[2] = {64, kRows};
+    cuuint32_t box[2] = {kStageK, kRows};
     cuuint32_t estr[2] = {1, 1};
     if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(a.Wq), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return WSW_ERR_CUDA;
-    const int m_tiles = static_cast<int>((a.Mo + kRows - 1) / kRows);
     const size_t smem = sizeof(Smem) + 1024;
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(moe_q8_tc_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return WSW_ERR_CUDA;
-    e = launch(moe_q8_tc_kernel, dim3(static_cast<unsigned>(a.E * m_tiles)), dim3(kThreadsM), smem, s, pdl, map, a,
-               m_tiles);
+    e = launch(moe_q8_tc_kernel, dim3(static_cast<unsigned>(sm_count)), dim3(kThreads), smem, s, pdl, map, a);
     return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
 }
 

@@ -23,7 +23,7 @@ struct MoeTcArgs {
 bool moe_q8_tc_supported(int64_t E, int64_t Mo, int64_t K, int64_t R, const void *Wq, const void *Wd,
                          const void *xq, const void *xd);
 
-// Launch it; returns a wsw_status.
-int moe_q8_tc_launch(const MoeTcArgs &a, cudaStream_t s, bool pdl);
+// Launch it (one persistent CTA per SM); returns a wsw_status.
+int moe_q8_tc_launch(const MoeTcArgs &a, int sm_count, cudaStream_t s, bool pdl);
 
 }  // namespace wsw
