@@ -128,6 +128,14 @@ __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// The CTA's threads request the 128-byte lines of [p, p + bytes) into L2, one line each.
+__device__ __forceinline__ void prefetch_range_l2(const void *p, int64_t bytes) {
+    const uintptr_t first = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(127);
+    const uintptr_t end = reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(bytes);
+    for (uintptr_t l = first + 128 * static_cast<uintptr_t>(threadIdx.x); l < end; l += 128 * blockDim.x)
+        prefetch_l2(reinterpret_cast<const void *>(l));
+}
+
 // bf16 pair in one 32-bit word -> two fp32 values (exact).
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }

@@ -44,6 +44,7 @@ struct Bf16 {
         return reinterpret_cast<const char *>(a.W + row * a.ld);
     }
     __device__ __forceinline__ static int64_t row_bytes(const Args &a) { return a.K * 2; }
+    __device__ __forceinline__ static void prefetch_x(const Args &a) { prefetch_range_l2(a.x, 4 * a.K); }
     struct Buf { uint32_t w[8]; };
     struct Acc { float a0, a1; };
     struct XVal { float4 q[4]; };

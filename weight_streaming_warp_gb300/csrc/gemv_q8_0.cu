@@ -74,6 +74,10 @@ struct Q8 {
         for (int i = 0; i < 8; ++i) b.w[i] = 0u;
         b.d = 0u;
     }
+    __device__ __forceinline__ static void prefetch_x(const Args &a) {
+        prefetch_range_l2(a.xq, a.K);
+        prefetch_range_l2(a.xd, a.K / 16);
+    }
     // Shared memory: xq as two planes of 16-byte halves [2][nsteps * 32], then xd.
     template <bool XS>
     __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
@@ -131,6 +135,7 @@ struct Q8X : Q8 {
         int8_t *xq_out;    // optional (with xd_out): q of x, K bytes
         uint16_t *xd_out;  // optional: binary16 scales, K / 32
     };
+    __device__ __forceinline__ static void prefetch_x(const Args &a) { prefetch_range_l2(a.x, 4 * a.K); }
     template <bool XS>
     __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
         constexpr int kB = 2;  // passes whose x loads are in flight together

@@ -27,7 +27,8 @@
 // never a result bit.
 //
 // Format policy F provides Args (with a Common c), Buf, Acc, XVal, the warps per CTA,
-// and load / row_ptr / row_bytes / stage_x / load_x / accumulate / lane_total / store.
+// and load / row_ptr / row_bytes / prefetch_x / stage_x / load_x / accumulate /
+// lane_total / store.
 // A step is 1 KB of a row in both formats.
 #pragma once
 
@@ -146,9 +147,12 @@ __global__ void __launch_bounds__(F::kWarps * 32, 16 / F::kWarps) stream_gemv_ke
             }
         };
 
-        // Both register batches are in flight before the dependency wait, i.e.
+        // The activation's lines are requested into L2 first (L2 is the point of
+        // coherence, so this is safe while the previous kernel may still write them);
+        // both register batches are then in flight before the dependency wait, i.e.
         // while the previous kernel in the stream drains, and the steps after them are
         // on their way into L2.
+        if (!started) F::prefetch_x(a);
         issue(bufA);
         issue(bufB);
         if (!started) {
