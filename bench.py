@@ -245,8 +245,9 @@ def _time_graph(torch, g, reps):
     return e0.elapsed_time(e1) / 1000.0 / reps
 
 
-KERNEL_SOURCES = {"gemv_q8_0": ("gemv_q8_0.cu", "stream_gemv.cuh", "common.cuh"),
-                  "quantize_gemv_q8_0": ("gemv_q8_0.cu", "stream_gemv.cuh", "q8_math.cuh", "common.cuh")}
+KERNEL_SOURCES = {"gemv_q8_0": ("gemv_q8_0.cu", "stream_gemv.cuh", "q8_dot.cuh", "q8_math.cuh", "common.cuh"),
+                  "quantize_gemv_q8_0": ("gemv_q8_0.cu", "stream_gemv.cuh", "q8_dot.cuh", "q8_math.cuh",
+                                         "common.cuh")}
 
 
 def kernel_source_sha(name):
