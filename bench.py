@@ -370,9 +370,15 @@ def _graph_rate(torch, fn, n, reps=5):
     return statistics.median(_time_graph(torch, g, 1) for _ in range(reps)) / n
 
 
+def _rate_both(torch, make_fn, n):
+    """Seconds per call of back-to-back calls in a graph, plain and PDL-linked."""
+    return _graph_rate(torch, make_fn(0), n), _graph_rate(torch, make_fn(1), n)
+
+
 def measure_rows(torch, wsw, dev):
     """The other hot-path calls on their configured shapes (graph-amortised, inputs
-    rotating over copies larger than L2 where a single copy would fit)."""
+    rotating over copies larger than L2 where a single copy would fit).  Each is timed
+    as plain back-to-back launches ("us") and PDL-linked ones ("us_pdl")."""
     import weight_streaming_warp_gb300.synthetic as syn
     g = torch.Generator(device=dev)
     g.manual_seed(2)
@@ -387,13 +393,17 @@ def measure_rows(torch, wsw, dev):
             Y = torch.empty((N, Mg), dtype=torch.float32, device=dev)
             it = [0]
 
-            def fn(stream, X=X, Y=Y, Wl=Wl):
-                wsw.gemm_bf16(Wl[it[0] % len(Wl)], X, out=Y)
-                it[0] += 1
-            t = _graph_rate(torch, fn, 24)
+            def make(pdl, X=X, Y=Y, Wl=Wl):
+                def fn(stream):
+                    wsw.gemm_bf16(Wl[it[0] % len(Wl)], X, out=Y, opts={"pdl": pdl})
+                    it[0] += 1
+                return fn
+            t, tp = _rate_both(torch, make, 24)
             key = "gemm_bf16_N%d_%s" % (N, "packed" if ld == Kg else "padded")
+            nbytes = Mg * Kg * 2 + N * Kg * 2 + N * Mg * 4
             out[key] = {"us": round(t * 1e6, 2), "TFLOPs": round(2.0 * N * Mg * Kg / t / 1e12, 2),
-                        "GBps": round((Mg * Kg * 2 + N * Kg * 2 + N * Mg * 4) / t / 1e9, 1)}
+                        "GBps": round(nbytes / t / 1e9, 1), "us_pdl": round(tp * 1e6, 2),
+                        "TFLOPs_pdl": round(2.0 * N * Mg * Kg / tp / 1e12, 2), "GBps_pdl": round(nbytes / tp / 1e9, 1)}
         del Wl
     del Ws
     # q8_0 KV cache dequant, 4 heads x 128
@@ -404,13 +414,16 @@ def measure_rows(torch, wsw, dev):
         o = torch.empty((4, depth, 128), dtype=torch.float16, device=dev)
         it = [0]
 
-        def fn(stream, qs=qs, ds=ds, o=o):
-            i = it[0] % copies
-            wsw.dequant_q8_0_kv(qs[i], ds[i], out=o)
-            it[0] += 1
-        t = _graph_rate(torch, fn, 32)
+        def make(pdl, qs=qs, ds=ds, o=o):
+            def fn(stream):
+                i = it[0] % copies
+                wsw.dequant_q8_0_kv(qs[i], ds[i], out=o, opts={"pdl": pdl})
+                it[0] += 1
+            return fn
+        t, tp = _rate_both(torch, make, 32)
         nb = depth * 4 * 128 * (1 + 2) + depth * 4 * 4 * 2
-        out["dequant_kv_d%d" % depth] = {"us": round(t * 1e6, 2), "GBps": round(nb / t / 1e9, 1)}
+        out["dequant_kv_d%d" % depth] = {"us": round(t * 1e6, 2), "GBps": round(nb / t / 1e9, 1),
+                                         "us_pdl": round(tp * 1e6, 2), "GBps_pdl": round(nb / tp / 1e9, 1)}
         del qs, ds
     # grouped MoE mat-vec (gate_up: 1536 x 2048 per expert), 128 experts, top-8; calls
     # rotate over 8 routings and 2 copies of the expert weights (2 x 403 MB), so the
@@ -427,14 +440,17 @@ def measure_rows(torch, wsw, dev):
         y = torch.empty((R, Mo), dtype=torch.float32, device=dev)
         it = [0]
 
-        def fn(stream, idss=idss, xq=xq, xd=xd, y=y, it=it):
-            i = it[0]
-            it[0] += 1
-            wsw.moe_gemv_q8_0(Wqs[i % nw], Wds[i % nw], xq, xd, idss[i % nr], out=y)
-        t = _graph_rate(torch, fn, 8 if T == 512 else 32)
+        def make(pdl, idss=idss, xq=xq, xd=xd, y=y, it=it):
+            def fn(stream):
+                i = it[0]
+                it[0] += 1
+                wsw.moe_gemv_q8_0(Wqs[i % nw], Wds[i % nw], xq, xd, idss[i % nr], out=y, opts={"pdl": pdl})
+            return fn
+        t, tp = _rate_both(torch, make, 8 if T == 512 else 32)
         used = statistics.mean(len(set(ids.tolist())) for ids in idss)
         nb = used * (Mo * Km + Mo * Km // 16) + R * (Km + Km // 16) + R * Mo * 4
         out["moe_gate_up_T%d" % T] = {"us": round(t * 1e6, 2), "experts_used": used, "GBps": round(nb / t / 1e9, 1),
+                                     "us_pdl": round(tp * 1e6, 2), "GBps_pdl": round(nb / tp / 1e9, 1),
                                      "note": "weights of the used experts once + activations + y; "
                                              "8 routings x 2 weight copies rotate"}
     del Wqs, Wds

@@ -172,3 +172,40 @@ def test_tensor_core_form_against_oracle(orc, Mo, K, T, En, topk):
             continue
         e = ids[m]
         check_tol(yc[m], y64[m], mag_q8(Wq[e], Wd[e], xq[m], xd[m]), TOL_Q8, "row %d" % m)
+
+
+@pytest.mark.parametrize("Mo,K,R", [(63, 96, 16), (256, 1024, 5), (1536, 2048, 1)])
+def test_few_rows_gathered_form(orc, Mo, K, R):
+    """At most 16 routed rows: each row streams its own expert (a repeated expert is
+    read twice).  Rows equal the dense mat-vec on their expert bit for bit for every
+    launch option; a bad id sets the flag and leaves its row untouched."""
+    wsw = need_gpu()
+    En = 6
+    g = np.random.default_rng(Mo * 7 + R)
+    Wq = g.integers(-127, 128, size=(En, Mo, K)).astype(np.int8)
+    Wd = g.integers(0x0800, 0x1c00, size=(En, Mo, K // 32)).astype(np.uint16)
+    xq = g.integers(-127, 128, size=(R, K)).astype(np.int8)
+    xd = g.integers(0x0800, 0x1c00, size=(R, K // 32)).astype(np.uint16)
+    ids = g.integers(0, En, size=R).astype(np.int32)
+    if R > 2:
+        ids[1] = ids[0]   # a repeated expert
+        ids[R - 1] = En   # out of range
+    Wqd, Wdd = torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda()
+    xqd, xdd = torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda()
+    ref = None
+    for opts in (None, {"rows_per_warp": 1}, {"rows_per_warp": 4, "load_bytes": 8}, {"pdl": 1, "ctas_per_sm": 1}):
+        y = torch.full((R, Mo), 7.0, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        wsw.moe_gemv_q8_0(Wqd, Wdd, xqd, xdd, torch.from_numpy(ids).cuda(), out=y, err_flag=err, opts=opts)
+        if ref is None:
+            ref = y.clone()
+        assert torch.equal(y.view(torch.int32), ref.view(torch.int32)), opts
+        assert (err.item() != 0) == bool((ids >= En).any())
+    for m in range(R):
+        if ids[m] >= En:
+            assert (ref[m] == 7.0).all()
+            continue
+        yd = wsw.gemv_q8_0(Wqd[ids[m]], Wdd[ids[m]], xqd[m], xdd[m])
+        assert torch.equal(yd.view(torch.int32), ref[m].view(torch.int32)), m
+        check_tol(ref[m].cpu().numpy(), orc.gemv_q8_0(Wq[ids[m]], Wd[ids[m]], xq[m], xd[m]),
+                  mag_q8(Wq[ids[m]], Wd[ids[m]], xq[m], xd[m]), TOL_Q8, "row %d" % m)

@@ -116,20 +116,36 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
-            pdl_wait();  // X is written by earlier kernels
-            for (int i = 0; i < nk && ok; ++i) {
+            // stage i: W boxes (consecutive 128-byte pieces of each weight row, requested
+            // back to back) and X boxes, both counted by full[i % stages]
+            auto load_w = [&](int i) {
+                const int s = i % stages, k = (kb0 + i) * kAtom * atoms;
+                for (int j = 0; j < atoms; ++j)
+                    tma_load_2d(sA + static_cast<size_t>(s) * a_bytes + j * kAtomA, &tmW, k + j * kAtom,
+                                static_cast<int>(m0), &full[s], pol_w);
+            };
+            auto load_x = [&](int i) {
+                const int s = i % stages, k = (kb0 + i) * kAtom * atoms;
+                for (int j = 0; j < atoms; ++j)
+                    tma_load_2d(sB + static_cast<size_t>(s) * b_bytes + j * (nt * kAtom * 2), &tmX, k + j * kAtom, n0,
+                                &full[s], pol_x);
+            };
+            // The weights do not come from earlier kernels: the first ring of W stages is
+            // in flight before the dependency wait, X (written by earlier kernels) after it.
+            const int pre = nk < stages ? nk : stages;
+            for (int i = 0; i < pre; ++i) {
+                mbar_expect_tx(&full[i], a_bytes + b_bytes);
+                load_w(i);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i) load_x(i);
+            for (int i = pre; i < nk && ok; ++i) {
                 const int s = i % stages;
                 const uint32_t round = static_cast<uint32_t>(i / stages);
                 if (!mbar_wait(&empty[s], (round & 1u) ^ 1u)) { ok = false; break; }
                 mbar_expect_tx(&full[s], a_bytes + b_bytes);
-                const int k = (kb0 + i) * kAtom * atoms;
-                // consecutive 128-byte pieces of each weight row are requested back to back
-                for (int j = 0; j < atoms; ++j)
-                    tma_load_2d(sA + static_cast<size_t>(s) * a_bytes + j * kAtomA, &tmW, k + j * kAtom,
-                                static_cast<int>(m0), &full[s], pol_w);
-                for (int j = 0; j < atoms; ++j)
-                    tma_load_2d(sB + static_cast<size_t>(s) * b_bytes + j * (nt * kAtom * 2), &tmX, k + j * kAtom, n0,
-                                &full[s], pol_x);
+                load_w(i);
+                load_x(i);
             }
         }
         __syncwarp();
@@ -181,6 +197,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         }
     }
 
+    pdl_launch_dependents();
     if (S > 1) {
         // Split-K: every rank adds a slice of the tile from all ranks, in rank order.
         cluster_sync();
@@ -219,7 +236,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         }
         cluster_sync();  // peers keep their shared memory until every rank has read it
     }
-    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -32,6 +32,7 @@ struct Bf16 {
     static constexpr int kWarps = 16;  // warps per CTA
     static constexpr int kStepElems = 512;
     static constexpr bool kGlobalX = true;  // x may be read through L1 instead of staged
+    static constexpr bool kWaitFirst = false;
     struct Args {
         sg::Common c;
         const uint16_t *W;
@@ -98,7 +99,7 @@ struct Bf16 {
     }
     template <bool XS>
     __device__ __forceinline__ static XVal load_x(const Args &a, const unsigned char *xsm, int step, int lane,
-                                                  int nsteps) {
+                                                  int nsteps, int64_t) {
         XVal v;
         const int64_t c = static_cast<int64_t>(step) * 32 + lane;
         if constexpr (XS) {

@@ -39,6 +39,7 @@ struct Q8 {
     static constexpr int kWarps = 8;  // warps per CTA
     static constexpr int kStepElems = 1024;
     static constexpr bool kGlobalX = false;  // x is always staged in shared memory
+    static constexpr bool kWaitFirst = false;
     struct Args {
         sg::Common c;
         const int8_t *Wq;
@@ -105,7 +106,7 @@ struct Q8 {
     }
     template <bool XS>
     __device__ __forceinline__ static XVal load_x(const Args &, const unsigned char *xsm, int step, int lane,
-                                                  int nsteps) {
+                                                  int nsteps, int64_t = 0) {
         const uint4 *xs = reinterpret_cast<const uint4 *>(xsm);
         const int64_t nslots = static_cast<int64_t>(nsteps) * 32;
         const uint16_t *xs_d = reinterpret_cast<const uint16_t *>(xs + 2 * nslots);
@@ -198,6 +199,74 @@ struct Q8X : Q8 {
     }
 };
 
+// The grouped MoE mat-vec for a few routed rows (wsw_moe_gemv_q8_0 with R <= 16): a
+// dense mat-vec over R * Mo virtual rows, virtual row v = m * Mo + o multiplying row o of
+// expert ids[m] with activation row m, so that y[m][o] = y[v] in the caller's [R][Mo]
+// layout.  Nothing is bucketed: every routed row streams its expert's rows (a repeated
+// expert among so few rows is read again).  The weight addresses come from the ids, which
+// an earlier kernel writes, so the dependency wait comes first (kWaitFirst).  The rows per
+// warp divide Mo and the K-segments are the dense model's for one Mo x K matrix, so every
+// row equals wsw_gemv_q8_0 on its expert, bit for bit.
+constexpr int kGatherMaxRows = 16;
+
+struct Q8G : Q8 {
+    static constexpr bool kWaitFirst = true;
+    struct Args : Q8::Args {
+        int64_t E, Mo;
+        const int32_t *ids;
+        int64_t R;
+        int32_t *err;
+    };
+    // the routing ids of this launch (-1 for an id outside [0, E)), staged per CTA
+    __device__ __forceinline__ static int *ids_smem() {
+        __shared__ int ids_s[kGatherMaxRows];
+        return ids_s;
+    }
+    // per-token bytes of the staged activation: Q8's two 16-byte planes and the scales
+    __device__ __forceinline__ static int64_t token_bytes(int nsteps) { return static_cast<int64_t>(nsteps) * 1088; }
+    __device__ __forceinline__ static int64_t expert_row(const Args &a, int64_t v, bool &valid) {
+        const int64_t m = v / a.Mo;
+        const int e = ids_smem()[m];
+        valid = e >= 0;
+        return static_cast<int64_t>(valid ? e : 0) * a.Mo + (v - m * a.Mo);
+    }
+    __device__ __forceinline__ static const char *row_ptr(const Args &a, int64_t v) {
+        bool valid;
+        return reinterpret_cast<const char *>(a.Wq + expert_row(a, v, valid) * a.ldq);
+    }
+    template <int LB>
+    __device__ __forceinline__ static void load(const Args &a, int64_t v, int step, int lane, Buf &b, uint64_t pol) {
+        bool valid;
+        const int64_t row = expert_row(a, v, valid);
+        if (valid) Q8::load<LB>(a, row, step, lane, b, pol);
+        else Q8::zero(b);
+    }
+    __device__ __forceinline__ static void prefetch_x(const Args &) {}
+    template <bool XS>
+    __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
+        if (threadIdx.x < a.R) {
+            const int e = a.ids[threadIdx.x];
+            const bool ok = e >= 0 && e < a.E;
+            ids_smem()[threadIdx.x] = ok ? e : -1;
+            if (!ok && blockIdx.x == 0 && a.err) atomicOr(a.err, 1);
+        }
+        for (int64_t m = 0; m < a.R; ++m) {
+            Q8::Args t = a;
+            t.xq = a.xq + m * a.K;
+            t.xd = a.xd + m * (a.K / 32);
+            Q8::stage_x<XS>(t, xsm + m * token_bytes(nsteps), nsteps);
+        }
+    }
+    template <bool XS>
+    __device__ __forceinline__ static XVal load_x(const Args &a, const unsigned char *xsm, int step, int lane,
+                                                  int nsteps, int64_t row) {
+        return Q8::load_x<XS>(a, xsm + (row / a.Mo) * token_bytes(nsteps), step, lane, nsteps);
+    }
+    __device__ __forceinline__ static void store(const Args &a, int64_t v, float s) {
+        if (ids_smem()[v / a.Mo] >= 0) a.y[v] = s;
+    }
+};
+
 // Dense launch shared by the two entry points (arguments already validated).
 template <class F>
 int q8_dense_launch(typename F::Args &a, int64_t M, int64_t K, const Opts &o, const DeviceInfo &di,
@@ -216,6 +285,30 @@ int q8_dense_launch(typename F::Args &a, int64_t M, int64_t K, const Opts &o, co
 }
 
 }  // namespace
+
+bool moe_q8_gather_takes(int64_t R) { return R > 0 && R <= kGatherMaxRows; }
+
+int moe_q8_gather_launch(const int8_t *Wq, const uint16_t *Wd, int64_t E, int64_t Mo, int64_t K, const int8_t *xq,
+                         const uint16_t *xd, const int32_t *ids, int64_t R, float *y, int32_t *err, const Opts &o,
+                         const DeviceInfo &di, cudaStream_t s) {
+    Q8G::Args a;
+    a.Wq = Wq; a.Wd = Wd; a.K = K; a.ldq = K; a.xq = xq; a.xd = xd; a.y = y;
+    a.E = E; a.Mo = Mo; a.ids = ids; a.R = R; a.err = err;
+    const int64_t nsteps = (K + Q8::kStepElems - 1) / Q8::kStepElems;
+    // rows of a warp never straddle two routed rows; the K-segments are those of one
+    // expert's dense Mo x K mat-vec (neither choice changes a bit of a row)
+    const int rw = Mo % o.rows_per_warp == 0 ? o.rows_per_warp : 1;
+    const int ls = sg::choose_log2_seg(Mo, static_cast<int>(nsteps), di.sm_count, Q8::kWarps);
+    a.c = sg::make_common_seg(R * Mo, static_cast<int>(nsteps), rw, Q8G::kWarps, ls);
+    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 16 / Q8G::kWarps;
+    const unsigned ctas = sg::grid_ctas(a.c, static_cast<int64_t>(di.sm_count) * cps);
+    const size_t x_smem = static_cast<size_t>(R) * static_cast<size_t>(nsteps) * 1088;
+    if (sg::kMaxPartials * 4 + x_smem > static_cast<size_t>(di.max_smem_optin)) return WSW_ERR_UNSUPPORTED;
+    int lb = load_width(Wq, K, o.load_bytes);
+    const cudaError_t e = sg::launch_stream_gemv<Q8G>(rw, lb, true, a, ctas, x_smem, s, o.pdl);
+    return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
+}
+
 }  // namespace wsw
 
 extern "C" int wsw_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, int64_t K, int64_t ldq,

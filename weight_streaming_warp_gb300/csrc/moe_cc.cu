@@ -384,6 +384,10 @@ extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E
     DeviceInfo di;
     if (!device_info(&di, &st)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (moe_q8_gather_takes(R)) {
+        const int gs = moe_q8_gather_launch(Wq, Wd, E, Mo, K, xq, xd, ids, R, y, err_flag, o, di, s);
+        if (gs != WSW_ERR_UNSUPPORTED) return gs;
+    }
     if (R > kTcMinRows && moe_q8_tc_supported(E, Mo, K, R, Wq, Wd, xq, xd)) {
         MoeTcArgs t;
         t.Wq = Wq; t.Wd = Wd; t.E = E; t.Mo = Mo; t.K = K; t.xq = xq; t.xd = xd; t.ids = ids; t.R = R;

@@ -1,9 +1,12 @@
-// moe_tc.cuh -- the tensor-core form of the grouped q8_0 MoE mat-vec (moe_tc.cu), used
-// by wsw_moe_gemv_q8_0 for problems with many rows.
+// moe_tc.cuh -- the forms of the grouped q8_0 MoE mat-vec that wsw_moe_gemv_q8_0 (moe_cc.cu)
+// dispatches to besides its own: the tensor-core form (moe_tc.cu) for many routed rows
+// and the gathered dense form (gemv_q8_0.cu) for a few.
 #pragma once
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include "common.cuh"
 
 namespace wsw {
 
@@ -25,5 +28,12 @@ bool moe_q8_tc_supported(int64_t E, int64_t Mo, int64_t K, int64_t R, const void
 
 // Launch it (one persistent CTA per SM); returns a wsw_status.
 int moe_q8_tc_launch(const MoeTcArgs &a, int sm_count, cudaStream_t s, bool pdl);
+
+// The form for a few routed rows (gemv_q8_0.cu): a dense mat-vec over R * Mo gathered
+// rows, each bit-identical to wsw_gemv_q8_0 on its expert.
+bool moe_q8_gather_takes(int64_t R);
+int moe_q8_gather_launch(const int8_t *Wq, const uint16_t *Wd, int64_t E, int64_t Mo, int64_t K, const int8_t *xq,
+                         const uint16_t *xd, const int32_t *ids, int64_t R, float *y, int32_t *err, const Opts &o,
+                         const DeviceInfo &di, cudaStream_t s);
 
 }  // namespace wsw

@@ -28,7 +28,10 @@
 //
 // Format policy F provides Args (with a Common c), Buf, Acc, XVal, the warps per CTA,
 // and load / row_ptr / row_bytes / prefetch_x / stage_x / load_x / accumulate /
-// lane_total / store.
+// lane_total / store.  load_x also receives the first row of the group (a format whose
+// activation differs by row picks it from there).  kWaitFirst: the weight addresses
+// depend on data written by earlier kernels, so the dependency wait and stage_x come
+// before the first weight load.
 // A step is 1 KB of a row in both formats.
 #pragma once
 
@@ -152,6 +155,15 @@ __global__ void __launch_bounds__(F::kWarps * 32, 16 / F::kWarps) stream_gemv_ke
         // both register batches are then in flight before the dependency wait, i.e.
         // while the previous kernel in the stream drains, and the steps after them are
         // on their way into L2.
+        if constexpr (F::kWaitFirst) {
+            if (!started) {
+                pdl_wait();
+                F::template stage_x<XS>(a, xsm, nsteps);
+                __syncthreads();
+                pdl_launch_dependents();
+                started = true;
+            }
+        }
         if (!started) F::prefetch_x(a);
         issue(bufA);
         issue(bufB);
@@ -188,7 +200,7 @@ __global__ void __launch_bounds__(F::kWarps * 32, 16 / F::kWarps) stream_gemv_ke
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (cq < nq) {
-                    const typename F::XVal xv = F::template load_x<XS>(a, xsm, cst, lane, nsteps);
+                    const typename F::XVal xv = F::template load_x<XS>(a, xsm, cst, lane, nsteps, cg * R);
 #pragma unroll
                     for (int r = 0; r < R; ++r) F::accumulate(acc[r], buf[u][r], xv);
                     if (++cst == cse) {
@@ -283,18 +295,22 @@ inline int choose_log2_seg(int64_t M, int nsteps, int sm_count, int nw) {
 // Host side: fill Common for M rows of `nsteps` steps, R rows per warp group and CTAs
 // of nw warps; the K-segments follow the model for CTAs of seg_nw warps (the format's
 // own width, so that a variant with other CTAs computes the same bits).
-inline Common make_common(int64_t M, int nsteps, int R, int sm_count, int nw, int seg_nw) {
+inline Common make_common_seg(int64_t M, int nsteps, int R, int nw, int log2_seg) {
     Common c;
     c.M = M;
     c.groups = (M + R - 1) / R;
     c.nsteps = nsteps;
-    c.log2_seg = choose_log2_seg(M, nsteps, sm_count, seg_nw);
+    c.log2_seg = log2_seg;
     const int lw = log2_warps(nw);
     c.log2_block = c.log2_seg > lw ? c.log2_seg : lw;
     const int64_t S = int64_t(1) << c.log2_seg, B = int64_t(1) << c.log2_block;
     c.nblocks = (c.groups * S + B - 1) / B;
     c.batch_blocks = static_cast<int>(kMaxPartials / (B * R));
     return c;
+}
+
+inline Common make_common(int64_t M, int nsteps, int R, int sm_count, int nw, int seg_nw) {
+    return make_common_seg(M, nsteps, R, nw, choose_log2_seg(M, nsteps, sm_count, seg_nw));
 }
 
 // CTAs of a launch: at most max_ctas, and no more than needed for every CTA to take
