@@ -438,13 +438,16 @@ def measure_rows(torch, wsw, dev):
         xq = torch.randint(-127, 128, (R, Km), dtype=torch.int8, device=dev, generator=g)
         xd = torch.rand((R, Km // 32), device=dev, generator=g).half()
         y = torch.empty((R, Mo), dtype=torch.float32, device=dev)
+        nws = wsw.moe_workspace_bytes(E, Km, R)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else False
         it = [0]
 
-        def make(pdl, idss=idss, xq=xq, xd=xd, y=y, it=it):
+        def make(pdl, idss=idss, xq=xq, xd=xd, y=y, it=it, ws=ws):
             def fn(stream):
                 i = it[0]
                 it[0] += 1
-                wsw.moe_gemv_q8_0(Wqs[i % nw], Wds[i % nw], xq, xd, idss[i % nr], out=y, opts={"pdl": pdl})
+                wsw.moe_gemv_q8_0(Wqs[i % nw], Wds[i % nw], xq, xd, idss[i % nr], out=y, opts={"pdl": pdl},
+                                  ws=ws)
             return fn
         t, tp = _rate_both(torch, make, 8 if T == 512 else 32)
         used = statistics.mean(len(set(ids.tolist())) for ids in idss)

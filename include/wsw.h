@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define WSW_ABI_VERSION 1
+#define WSW_ABI_VERSION 2
 
 typedef enum wsw_status {
     WSW_OK = 0,
@@ -179,6 +179,14 @@ int wsw_quantize_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, int6
                            const wsw_launch_opts *opts);
 
 /*
+ * wsw_moe_workspace_bytes -- bytes of device workspace that wsw_moe_gemv_q8_0 can use
+ * for E experts, row length K and R routed rows (0: that call needs none).  With the
+ * workspace, calls with more than 256 routed rows run on the tensor cores; without it
+ * they run on the CUDA cores.
+ */
+size_t wsw_moe_workspace_bytes(int64_t E, int64_t K, int64_t R);
+
+/*
  * wsw_moe_gemv_q8_0 -- grouped MoE mat-vec over per-expert q8_0 weights ([P3]
  * Cause and Scope: the MoE path quantizes m = T x top_k rows, then runs a grouped
  * GEMM over the experts).
@@ -186,10 +194,12 @@ int wsw_quantize_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, int6
  * For each row m < R with e = ids[m] in [0, E):
  *   y[m][o] = gemv_q8_0(W_e, x_m)[o],  o < Mo,
  * bit-identical to wsw_gemv_q8_0 on expert e's matrix and row m for R <= 256.
- * Each expert that some row uses is streamed from memory once per call; experts
- * no row uses are not read.  For R > 256 the rows of an expert are multiplied on
- * the tensor cores with exact integer block sums; results then agree with the
- * CUDA-core form within fp32 rounding, not bit for bit.
+ * Each expert that some row uses is streamed from memory once per call (for R <= 16
+ * each routed row streams its own expert, so a repeated expert is read again);
+ * experts no row uses are not read.  For R > 256 with a workspace, a prepass sorts
+ * and converts the activations into the workspace and the rows of an expert are
+ * multiplied on the tensor cores with exact integer block sums; results then agree
+ * with the CUDA-core form within fp32 rounding, not bit for bit.
  *
  *   Wq   int8 [E][Mo][K];  Wd binary16 [E][Mo][K/32];  K % 32 == 0.
  *   xq   int8 [R][K];  xd binary16 [R][K/32].
@@ -197,11 +207,16 @@ int wsw_quantize_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t M, int6
  *        row is left untouched, and *err_flag (if err_flag != NULL) is set to a
  *        nonzero value.  The library never clears *err_flag.
  *   y    fp32 [R][Mo].
+ *   ws   device workspace of ws_bytes >= wsw_moe_workspace_bytes(E, K, R) bytes,
+ *        256-byte aligned, owned by the caller and overwritten by the call; NULL (or
+ *        too small) keeps every row count on the CUDA cores.  Two calls in flight at
+ *        once need two workspaces.
  *   R <= 16384 and E <= 1024, else WSW_ERR_UNSUPPORTED.
  */
 int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E, int64_t Mo, int64_t K,
                       const int8_t *xq, const uint16_t *xd, const int32_t *ids, int64_t R,
-                      float *y, int32_t *err_flag, void *stream, const wsw_launch_opts *opts);
+                      float *y, int32_t *err_flag, void *ws, size_t ws_bytes, void *stream,
+                      const wsw_launch_opts *opts);
 
 /*
  * wsw_dequant_q8_0_kv -- dequantize one layer's q8_0 K (or V) cache once into a

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert wsw.abi_version() == 1
+    assert wsw.abi_version() == 2
     assert wsw.status_string(0) == "WSW_OK"
     assert wsw.status_string(1) == "WSW_ERR_INVALID_ARG"
     assert wsw.status_string(2) == "WSW_ERR_MISALIGNED"
@@ -91,10 +91,18 @@ def test_gemv_rejects_on_host(lib):
 
 def test_other_calls_reject_on_host(lib):
     m = lib.wsw_moe_gemv_q8_0
-    assert m(P(4096), P(4096), 8, 16, 48, P(4096), P(4096), P(4096), 4, P(4096), None, None, None) == INVALID
-    assert m(P(4096), P(4096), 4096, 16, 64, P(4096), P(4096), P(4096), 4, P(4096), None, None, None) == UNSUPPORTED
-    assert m(P(4096), P(4096), 8, 16, 64, P(4096), P(4096), P(4096), 70000, P(4096), None, None, None) == UNSUPPORTED
-    assert m(P(4096), P(4096), 8, 16, 64, P(4096), P(4096), P(4096), 0, P(4096), None, None, None) == 0
+    assert m(P(4096), P(4096), 8, 16, 48, P(4096), P(4096), P(4096), 4, P(4096), None, None, 0, None, None) == INVALID
+    assert m(P(4096), P(4096), 4096, 16, 64, P(4096), P(4096), P(4096), 4, P(4096), None, None, 0, None,
+             None) == UNSUPPORTED
+    assert m(P(4096), P(4096), 8, 16, 64, P(4096), P(4096), P(4096), 70000, P(4096), None, None, 0, None,
+             None) == UNSUPPORTED
+    assert m(P(4096), P(4096), 8, 16, 64, P(4096), P(4096), P(4096), 0, P(4096), None, None, 0, None, None) == 0
+    w = lib.wsw_moe_workspace_bytes
+    assert w(128, 2048, 16) == 0 and w(128, 2048, 256) == 0 and w(128, 96, 4096) == 0
+    # sorted positions (R + 3 per used expert, rounded to 4): fp16 rows, fp32 scales, list, header
+    n = w(128, 2048, 4096)
+    rp = 4096 + 3 * 128
+    assert n >= rp * 2048 * 2 + rp * 64 * 4 + rp * 2 and n % 256 == 0
     d = lib.wsw_dequant_q8_0_kv
     assert d(P(4096), P(4096), 16, 4, 100, P(4096), None, None) == INVALID
     assert d(P(4096), P(4097), 16, 4, 128, P(4096), None, None) == MISALIGNED

@@ -157,21 +157,23 @@ def test_tensor_core_form_against_oracle(orc, Mo, K, T, En, topk):
     ids[5] = En  # out of range
     x = syn.normal(4, "tc_x%d" % K, (R, K)).numpy()
     xq, xd = orc.quantize_q8(x, 32)
-    y = torch.full((R, Mo), float("nan"), device="cuda")
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    wsw.moe_gemv_q8_0(torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda(),
-                      torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda(),
-                      torch.from_numpy(ids).cuda(), out=y, err_flag=err)
-    yc = y.cpu().numpy()
-    assert err.item() != 0
-    assert np.isnan(yc[5]).all()
     y64, bad = orc.moe_gemv_q8_0(Wq, Wd, xq, xd, ids)
     assert bad == 1
-    for m in range(R):
-        if m == 5:
-            continue
-        e = ids[m]
-        check_tol(yc[m], y64[m], mag_q8(Wq[e], Wd[e], xq[m], xd[m]), TOL_Q8, "row %d" % m)
+    assert wsw.moe_workspace_bytes(En, K, R) > 0
+    for ws in (None, False):  # with the workspace (tensor cores) and without (CUDA cores)
+        y = torch.full((R, Mo), float("nan"), device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        wsw.moe_gemv_q8_0(torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda(),
+                          torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda(),
+                          torch.from_numpy(ids).cuda(), out=y, err_flag=err, ws=ws)
+        yc = y.cpu().numpy()
+        assert err.item() != 0
+        assert np.isnan(yc[5]).all()
+        for m in range(R):
+            if m == 5:
+                continue
+            e = ids[m]
+            check_tol(yc[m], y64[m], mag_q8(Wq[e], Wd[e], xq[m], xd[m]), TOL_Q8, "row %d (ws %s)" % (m, ws is None))
 
 
 @pytest.mark.parametrize("Mo,K,R", [(63, 96, 16), (256, 1024, 5), (1536, 2048, 1)])

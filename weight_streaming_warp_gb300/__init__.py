@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "LaunchOpts", "WswError", "library_path", "load", "quantize_q8", "gemv_bf16",
     "gemv_bf16_chain", "gemv_q8_0", "quantize_gemv_q8_0", "moe_gemv_q8_0", "dequant_q8_0_kv", "gemm_bf16",
-    "upload_padded", "status_string", "abi_version",
+    "upload_padded", "status_string", "abi_version", "moe_workspace_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -78,7 +78,9 @@ def load():
     L.wsw_gemv_bf16_chain.argtypes = [_i64, _p, _p, _p]
     L.wsw_gemv_q8_0.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p]
     L.wsw_quantize_gemv_q8_0.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p]
-    L.wsw_moe_gemv_q8_0.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p, _i64, _p, _p, _p, _p]
+    L.wsw_moe_gemv_q8_0.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p, _i64, _p, _p, _p, ctypes.c_size_t, _p, _p]
+    L.wsw_moe_workspace_bytes.argtypes = [_i64, _i64, _i64]
+    L.wsw_moe_workspace_bytes.restype = ctypes.c_size_t
     L.wsw_dequant_q8_0_kv.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p]
     L.wsw_gemm_bf16.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _p, _p]
     for f in ("wsw_quantize_q8", "wsw_gemv_bf16", "wsw_gemv_bf16_chain", "wsw_gemv_q8_0", "wsw_quantize_gemv_q8_0",
@@ -211,10 +213,17 @@ def quantize_gemv_q8_0(Wq, Wd, x, K=None, out=None, x_out=None, opts=None):
     return y
 
 
-def moe_gemv_q8_0(Wq, Wd, xq, xd, ids, out=None, err_flag=None, opts=None):
+def moe_workspace_bytes(E, K, R) -> int:
+    """Device workspace bytes that moe_gemv_q8_0 can use for these sizes (0: none)."""
+    return int(load().wsw_moe_workspace_bytes(E, K, R))
+
+
+def moe_gemv_q8_0(Wq, Wd, xq, xd, ids, out=None, err_flag=None, opts=None, ws=None):
     """Grouped q8_0 mat-vec.  Wq int8 [E][Mo][K], Wd fp16 [E][Mo][K/32], xq int8 [R][K],
     xd fp16 [R][K/32], ids int32 [R] -> y fp32 [R][Mo].  Rows with an id outside
-    [0, E) are skipped and set err_flag (an int32 device tensor) nonzero."""
+    [0, E) are skipped and set err_flag (an int32 device tensor) nonzero.  ws: a uint8
+    device tensor of at least moe_workspace_bytes(E, K, R) bytes; by default one is
+    allocated when the call can use it, ws=False runs without one."""
     _dev(Wq, torch.int8, "Wq")
     _dev(Wd, torch.float16, "Wd")
     _dev(xq, torch.int8, "xq")
@@ -227,9 +236,13 @@ def moe_gemv_q8_0(Wq, Wd, xq, xd, ids, out=None, err_flag=None, opts=None):
             raise WswError("%s must be contiguous" % nm)
     y = torch.empty((R, Mo), dtype=torch.float32, device=Wq.device) if out is None else out
     errp = err_flag.data_ptr() if err_flag is not None else None
+    if ws is None:
+        nbytes = moe_workspace_bytes(E, K, R)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=Wq.device) if nbytes else False
+    wsp, wsn = (ws.data_ptr(), ws.numel()) if ws is not False else (None, 0)
     _check(load().wsw_moe_gemv_q8_0(Wq.data_ptr(), Wd.data_ptr(), E, Mo, K, xq.data_ptr(),
-                                    xd.data_ptr(), ids.data_ptr(), R, y.data_ptr(), errp, _stream(),
-                                    _opts(opts)), "moe_gemv_q8_0")
+                                    xd.data_ptr(), ids.data_ptr(), R, y.data_ptr(), errp, wsp, wsn,
+                                    _stream(), _opts(opts)), "moe_gemv_q8_0")
     return y
 
 

@@ -363,9 +363,15 @@ cudaError_t launch_cc(bool split, const MoeArgs &a, unsigned ctas, size_t smem, 
 }  // namespace
 }  // namespace wsw
 
+extern "C" size_t wsw_moe_workspace_bytes(int64_t E, int64_t K, int64_t R) {
+    if (R <= wsw::kTcMinRows || K % 256 != 0) return 0;
+    return wsw::moe_q8_tc_workspace_bytes(E, K, R);
+}
+
 extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E, int64_t Mo, int64_t K,
                                  const int8_t *xq, const uint16_t *xd, const int32_t *ids, int64_t R,
-                                 float *y, int32_t *err_flag, void *stream, const wsw_launch_opts *opts) {
+                                 float *y, int32_t *err_flag, void *ws, size_t ws_bytes, void *stream,
+                                 const wsw_launch_opts *opts) {
     using namespace wsw;
     Opts o;
     int st = resolve_opts(opts, &o);
@@ -388,11 +394,11 @@ extern "C" int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E
         const int gs = moe_q8_gather_launch(Wq, Wd, E, Mo, K, xq, xd, ids, R, y, err_flag, o, di, s);
         if (gs != WSW_ERR_UNSUPPORTED) return gs;
     }
-    if (R > kTcMinRows && moe_q8_tc_supported(E, Mo, K, R, Wq, Wd, xq, xd)) {
+    if (R > kTcMinRows) {
         MoeTcArgs t;
         t.Wq = Wq; t.Wd = Wd; t.E = E; t.Mo = Mo; t.K = K; t.xq = xq; t.xd = xd; t.ids = ids; t.R = R;
-        t.y = y; t.err = err_flag;
-        return moe_q8_tc_launch(t, di.sm_count, s, o.pdl);
+        t.y = y; t.err = err_flag; t.ws = ws; t.ws_bytes = ws_bytes;
+        if (moe_q8_tc_supported(t)) return moe_q8_tc_launch(t, di.sm_count, s, o.pdl);
     }
     MoeArgs a;
     a.Wq = Wq; a.Wd = Wd; a.E = E; a.Mo = Mo; a.K = K; a.xq = xq; a.xd = xd; a.ids = ids; a.R = R;

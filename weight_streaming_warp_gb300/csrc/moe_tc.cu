@@ -6,44 +6,43 @@
 // contraction (about 60 integer operations per weight byte at T = 512), so it runs on
 // tcgen05 instead of dp4a.
 //
-// Exactness.  q8_0 values are integers in [-127, 127], exact in fp16.  The weights enter
-// the MMA as they are; an activation byte q enters biased, as the binary16 value 1152 + q
-// (its bit pattern is 0x6400 | (q ^ 0x80), two byte permutes per four values).  Each
-// block sum over 32 products is then I + 1152 * S with S the block's weight sum, at most
-// 32 * 127 * 1279 < 2^23 in magnitude, so every partial sum is an integer exact in the
-// fp32 accumulator.  One B row holds the constant 1152, so the MMA also yields the
-// correction 1152 * S in its own column.  One tcgen05.mma (kind::f16, K = 32 as two K = 16
-// steps) per block gives these exact sums for 128 weight rows x up to 62 routed rows; the
-// epilogue subtracts the correction, scales by fp32(Wd) * fp32(xd) and accumulates in fp32:
-//   y[m][o] = sum_b Wd[o][b] * xd[m][b] * isum_b(o, m).
+// Exactness.  q8_0 values are integers in [-127, 127], exact in fp16; a 32-value block
+// product sum is at most 32 * 127^2 < 2^24, exact in the fp32 accumulator.  So one
+// tcgen05.mma (kind::f16, K = 32 as two K = 16 steps) per block yields the exact integer
+// block sums of a 128-row x (up to) 64-token tile.  The epilogue scales each block sum by
+// fp32(Wd) * fp32(xd) (an exact product) and accumulates in fp32:
+//   y[m][o] = sum_b (Wd[o][b] * xd[m][b]) * isum_b(o, m).
 //
-// Persistent: one CTA per SM.  Every CTA buckets the routing ids by expert in shared
-// memory (the same stable lists in every CTA), then walks the work items i = blockIdx,
-// blockIdx + gridDim, ...; an item is (expert e, 128 output rows, up to 62 of e's routed
-// rows), items ordered by expert, then row tile, then token tile, so the grid streams
-// one contiguous window of the expert weights and the token tiles of one weight tile run
-// side by side (the second read of the tile comes from L2).  A stage is 128 K-values
-// (four blocks).  Warp roles (16 warps):
-//   warp 0       TMA: raw int8 weight tiles (128 rows x 128 bytes, 128-byte swizzle) into
-//                a ring of kRaw stages
-//   warp 1       tensor memory owner; one thread issues the MMAs: A from tensor memory,
-//                B from shared memory, D into a ring of kDPairs slots of two 64-column
-//                blocks, and commits once per pair
-//   warps 2-5    A converters: thread = weight row (its tensor-memory lane); reads its
-//                row's 128 bytes from the swizzled tile (conflict-free), converts int8 ->
-//                fp16 and writes the 64 packed columns with tcgen05.st
-//   warps 6-7    B converters: thread = B row (a routed row, or a constant row); its
-//                activation values by cp.async (one stage ahead), int8 -> biased fp16
-//                into 128-byte-swizzled K-major B tiles;
-//                halfway through an item they start the cp.async of the next item's
-//                scale rows (Wd rows as they are, padded; xd rows), and at its first stage
-//                turn the xd rows into fp32 [block][token]
-//   warps 8-15   epilogue: two groups of four warps (one per lane quarter); tcgen05.ld of
-//                a block, scale and accumulate; with at most 31 routed rows group h takes
-//                the blocks of parity h (columns 0-31) and hands its sums to group 0
-//                through shared memory, with more it takes every block for columns
-//                32 h .. 32 h + 31.  Columns 0-30 and 32-62 are routed rows, columns 31
-//                and 63 the corrections.
+// Two launches.
+//  * moe_q8_prep_kernel buckets the routing ids by expert (stable lists, each expert's
+//    run padded to a multiple of 4 positions so that every later TMA coordinate stays
+//    16-byte aligned) and writes into the caller's workspace, in that sorted order, the
+//    activations as exact fp16 (Xh [Rp][K]) and their scales as fp32, block-major
+//    (Xs [K/32][Rp]).  Each activation is converted once, not once per weight tile.
+//  * moe_q8_tc_kernel, persistent (one CTA per SM), walks the work items i = blockIdx,
+//    blockIdx + gridDim, ...; an item is (expert e, 128 output rows, up to 64 of e's
+//    routed rows), ordered by expert, then row tile, then token tile, so the grid streams
+//    one contiguous window of the expert weights.  A stage is 128 K-values (four blocks).
+//    Warp roles (16 warps):
+//      warp 0      TMA: raw int8 weight tiles (128 rows x 128 bytes, 128-byte swizzle)
+//                  into a ring of kRaw stages
+//      warp 1      tensor memory owner; one thread issues the MMAs: A from tensor memory,
+//                  B from shared memory, D into a ring of kDPairs slots of two 64-column
+//                  blocks.  Each barrier operation costs this thread about as much as an
+//                  MMA, so it waits twice and commits three times per stage (8 MMAs)
+//      warps 2-5   A converters: thread = weight row (its tensor-memory lane); reads its
+//                  row's 128 bytes from the swizzled tile (conflict-free), converts int8
+//                  -> fp16 and writes the 64 packed columns with tcgen05.st; they signal a
+//                  stage only once its B tile has landed too
+//      warp 6      TMA: the fp16 activation tile of each stage (64 sorted rows x 128
+//                  values, two 128-byte-swizzled atoms) into a ring of kBS slots, and
+//                  each item's scale tile
+//      warp 7      cp.async of each item's 128 Wd rows (padded rows in shared memory)
+//      warps 8-15  epilogue: two groups of four warps (one per lane quarter); tcgen05.ld
+//                  of a block, scale and accumulate; with at most 32 routed rows group h
+//                  takes the blocks of parity h and hands its sums to group 0 through
+//                  shared memory, with more it takes every block for columns 32 h ..
+//                  32 h + 31
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -58,45 +57,67 @@ namespace {
 using namespace tc;
 
 constexpr int kRows = 128;      // output rows per item (MMA M)
-constexpr int kCols = 64;       // B rows = accumulator columns of a block (MMA N <= 64)
-constexpr int kNT = 62;         // routed rows per item: columns 0-30 and 32-62
-constexpr int kHalf = 31;       // routed rows per 32-column half (column 31 / 63: correction)
+constexpr int kNT = 64;         // routed rows per item (MMA N <= 64)
 constexpr int kStageK = 128;    // K-values per stage (four blocks)
 constexpr int kRaw = 4;         // raw weight stages (16 KB each)
-constexpr int kAB = 2;          // A (tensor memory) and B (shared memory) slots
+constexpr int kAB = 2;          // A slots (tensor memory)
+constexpr int kBS = 3;          // B slots (shared memory): the activation tile of a stage
 constexpr int kDPairs = 3;      // accumulator slots of two blocks (64 columns each)
-constexpr int kXAhead = 2;      // activation cp.async ring (stages)
+constexpr int kDStageBars = 3;  // accumulator-full barriers, one per stage (a ring)
 constexpr int kMaxBlocks = 64;  // K <= 2048
-constexpr int kMaxList = 4096;  // routed rows kept in shared memory
+constexpr int kMaxRows = 4096;  // routed rows
 constexpr int kMaxE = 512;
+constexpr int kMaxSorted = kMaxRows + 3 * kMaxE;  // sorted positions with per-expert padding
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kBucketWarps = 8;
+constexpr int kPrepThreads = 512;
 
 constexpr int kRawBytes = kRows * kStageK;       // 16 KB
-constexpr int kBAtom = kCols * 128;              // one 64-value K-major atom of B: 8 KB
+constexpr int kBAtom = kNT * 128;                // one 64-value K-major atom of B: 8 KB
 constexpr int kBBytes = 2 * kBAtom;              // 16 KB
-constexpr int kXRawBytes = kCols * kStageK;      // 8 KB
-constexpr int kScalePitch = 144;                 // bytes per staged scale row (<= 64 binary16 + pad)
+constexpr int kScalePitch = 144;                 // bytes per staged Wd row (<= 64 binary16 + pad)
 constexpr uint32_t kACol = 0;                    // A slots: columns 0 .. 127
 constexpr uint32_t kDCol = 64 * kAB;             // D slots: columns 128 .. 511 (128 per pair)
 constexpr uint32_t kTmemCols = 512;
 
+// Workspace layout (byte offsets, each section 256-aligned).
+struct WsLayout {
+    int64_t Rp;         // sorted positions (a multiple of 4)
+    size_t hdr;         // int: nitems, then cnt[E], off[E], ibase[E + 1]
+    size_t list;        // int16 [Rp]: routed row at each sorted position, -1 for padding
+    size_t xh;          // fp16 [Rp][K]
+    size_t xs;          // fp32 [K/32][Rp]
+    size_t bytes;
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+WsLayout ws_layout(int64_t E, int64_t K, int64_t R) {
+    WsLayout L;
+    const int64_t pad = 3 * (E < R ? E : R);
+    L.Rp = (R + pad + 3) & ~int64_t(3);
+    L.hdr = 0;
+    L.list = align256(static_cast<size_t>(1 + 3 * E + 1) * 4);
+    L.xh = align256(L.list + static_cast<size_t>(L.Rp) * 2);
+    L.xs = align256(L.xh + static_cast<size_t>(L.Rp) * K * 2);
+    L.bytes = align256(L.xs + static_cast<size_t>(K / 32) * L.Rp * 4);
+    return L;
+}
+
 struct Smem {
-    unsigned char raw[kRaw][kRawBytes];     // 1024-aligned (first member); bucketing scratch first
-    unsigned char bt[kAB][kBBytes];         // 1024-aligned
-    unsigned char xraw[kXAhead][kXRawBytes];  // row t: 16-byte chunk j at (j ^ (t & 7))
+    unsigned char raw[kRaw][kRawBytes];        // 1024-aligned (first member)
+    unsigned char bt[kBS][kBBytes];            // 1024-aligned
     unsigned char wd[2][kRows * kScalePitch];  // per item (double-buffered): Wd rows, padded
-    unsigned char xdr[kCols * kScalePitch];   // the next item's xd rows, padded
-    float xs[2][kMaxBlocks][kCols];           // per item: xd as fp32, [block][column]
-    float comb[32][kRows];                    // group 1 -> group 0 partial sums (<= 32 rows)
-    uint16_t list[kMaxList];
+    float xs[2][kMaxBlocks][kNT];              // per item: xd as fp32, [block][token]
+    float comb[32][kRows];                     // group 1 -> group 0 partial sums (<= 32 rows)
+    int16_t list[kMaxSorted];
     int cnt[kMaxE];
     int off[kMaxE];
     int ibase[kMaxE + 1];
     uint64_t raw_full[kRaw], raw_empty[kRaw];
-    uint64_t a_full[kAB], b_full[kAB], ab_empty[kAB];
-    uint64_t d_full[kDPairs], d_empty[kDPairs];
+    uint64_t a_full[kAB], a_empty[kAB], b_full[kBS], b_empty[kBS];
+    uint64_t d_full[kDStageBars], d_empty[kDPairs];
     uint64_t s_full[2], s_empty[2];
     uint32_t tmem_slot;
     int nitems;
@@ -105,6 +126,23 @@ struct Smem {
 // byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled K-major tile
 __device__ __forceinline__ uint32_t sw_off(int r, int c) {
     return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Two fp32 lanes in one 64-bit register, for the packed fp32 instructions of sm_100+
+// (each lane rounds exactly as the scalar instruction does).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+// acc += (w * x) * d, lane by lane, with the product rounded before the fma
+__device__ __forceinline__ void f2_scale_fma(uint64_t &acc, uint64_t w, uint64_t x, uint64_t d) {
+    uint64_t s;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(w), "l"(x));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(s), "l"(d));
 }
 
 // 16 int8 values -> 16 fp16 values (exact), as 8 packed half2 words.  A byte q with its
@@ -162,7 +200,7 @@ __device__ __forceinline__ void mma_ts(uint32_t dtmem, uint32_t atmem, uint64_t 
 struct Item {
     int e;     // expert
     int m0;    // first output row
-    int tok0;  // first routed row in the expert-ordered list
+    int tok0;  // first sorted position of its routed rows
     int n;     // routed rows (1 .. kNT)
 };
 
@@ -178,61 +216,53 @@ __device__ __forceinline__ void decode_item(const Smem &S, int i, int &ecur, Ite
     it.n = c - tt * kNT < kNT ? c - tt * kNT : kNT;
 }
 
-// accumulator column of routed row t of an item, and back (-1: a correction column)
-__device__ __forceinline__ int col_of(int t) { return t < kHalf ? t : t + 1; }
-__device__ __forceinline__ int tok_of(int col) { return (col & 31) == kHalf ? -1 : (col < 32 ? col : col - 1); }
-// MMA N of an item with n routed rows: one half (and its correction) or both
-__device__ __forceinline__ int cols_of(int n) { return n <= kHalf ? 32 : 64; }
-
-// 16 int8 values -> 16 biased binary16 values 1152 + q (exact), as 8 packed half2 words
-__device__ __forceinline__ void i8x16_to_h_biased(const uint4 &v, uint32_t *o) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t u = w[i] ^ 0x80808080u;
-        o[2 * i] = __byte_perm(u, 0x64646464u, 0x4140);      // 1024 + u0, 1024 + u1
-        o[2 * i + 1] = __byte_perm(u, 0x64646464u, 0x4342);  // 1024 + u2, 1024 + u3
-    }
-}
-
-__global__ void __launch_bounds__(kThreads, 1)
-    moe_q8_tc_kernel(const __grid_constant__ CUtensorMap tmWq, const MoeTcArgs a) {
-    extern __shared__ unsigned char smem_raw[];
-    Smem &S = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+// ------------------------------------------------------------------- prepass --
+// Every CTA buckets the ids (the same stable lists everywhere), CTA 0 writes the header
+// and the sorted-position list, and every CTA converts its share of the routed rows.
+// Dynamic shared memory: ids[R], wcnt[kBucketWarps][E], cnt[E], off[E], pos[R] (ints).
+__global__ void __launch_bounds__(kPrepThreads) moe_q8_prep_kernel(const MoeTcArgs a, const WsLayout L) {
+    extern __shared__ int prep_smem[];
     const int E = static_cast<int>(a.E);
     const int R = static_cast<int>(a.R);
-    const int nb = static_cast<int>(a.K / 32);       // blocks per row
-    const int kst = static_cast<int>(a.K / kStageK); // stages per item
+    const int nb = static_cast<int>(a.K / 32);
     const int m_tiles = static_cast<int>((a.Mo + kRows - 1) / kRows);
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kRaw; ++i) { mbar_init(&S.raw_full[i], 1); mbar_init(&S.raw_empty[i], 128); }
-        for (int i = 0; i < kAB; ++i) {
-            mbar_init(&S.a_full[i], 128); mbar_init(&S.b_full[i], 64); mbar_init(&S.ab_empty[i], 1);
-        }
-        for (int i = 0; i < kDPairs; ++i) { mbar_init(&S.d_full[i], 1); mbar_init(&S.d_empty[i], 8); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&S.s_full[i], 64); mbar_init(&S.s_empty[i], 256); }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
+    int *ids_s = prep_smem;
+    int *wcnt = ids_s + R;
+    int *cnt = wcnt + kBucketWarps * E;
+    int *off = cnt + E;
+    int *pos = off + E;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    unsigned char *ws = static_cast<unsigned char *>(a.ws);
+    int *hdr = reinterpret_cast<int *>(ws + L.hdr);
+    int16_t *list = reinterpret_cast<int16_t *>(ws + L.list);
+    __half *xh = reinterpret_cast<__half *>(ws + L.xh);
+    float *xs = reinterpret_cast<float *>(ws + L.xs);
 
     pdl_wait();  // ids and activations come from earlier kernels
-
-    // ------------------------------------------------------------ bucketing
-    // Stable per-expert lists of the routed rows (every CTA builds the same ones).
-    int *ids_s = reinterpret_cast<int *>(&S.raw[0][0]);
-    int *wcnt = ids_s + R;  // [kBucketWarps][E]
+    pdl_launch_dependents();
     {
         bool bad = false;
-        for (int m = threadIdx.x; m < R; m += kThreads) {
+        const bool vec = (reinterpret_cast<uintptr_t>(a.ids) & 15) == 0;
+        const int nv = vec ? R / 4 : 0;  // ids read as int4 pieces, the rest one by one
+        for (int q = threadIdx.x; q < nv; q += kPrepThreads) {
+            const int4 v = __ldg(reinterpret_cast<const int4 *>(a.ids) + q);
+            const int t[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool ok = t[i] >= 0 && t[i] < E;
+                ids_s[4 * q + i] = ok ? t[i] : -1;
+                bad |= !ok;
+            }
+        }
+        for (int m = 4 * nv + threadIdx.x; m < R; m += kPrepThreads) {
             const int id = a.ids[m];
             const bool ok = id >= 0 && id < E;
             ids_s[m] = ok ? id : -1;
             bad |= !ok;
         }
         if (bad && blockIdx.x == 0 && a.err) atomicOr(a.err, 1);
-        for (int i = threadIdx.x; i < kBucketWarps * E; i += kThreads) wcnt[i] = 0;
+        for (int i = threadIdx.x; i < kBucketWarps * E; i += kPrepThreads) wcnt[i] = 0;
     }
     __syncthreads();
     const int r0 = warp < kBucketWarps ? static_cast<int>(static_cast<int64_t>(warp) * R / kBucketWarps) : 0;
@@ -245,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kThreads) {
+    for (int e = threadIdx.x; e < E; e += kPrepThreads) {
         int run = 0;
 #pragma unroll
         for (int w = 0; w < kBucketWarps; ++w) {
@@ -253,17 +283,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             wcnt[w * E + e] = run;
             run += c;
         }
-        S.cnt[e] = run;
+        cnt[e] = run;
     }
     __syncthreads();
     if (warp == 0) {
-        // exclusive scans over the experts: list offsets and item bases
+        // exclusive scans over the experts: padded offsets and item bases
         int run = 0, irun = 0;
         for (int base = 0; base < E; base += 32) {
             const int e = base + lane;
-            const int c = e < E ? S.cnt[e] : 0;
+            const int c = e < E ? cnt[e] : 0;
+            const int span = (c + 3) & ~3;
             const int items = m_tiles * ((c + kNT - 1) / kNT);
-            int incl = c, iincl = items;
+            int incl = span, iincl = items;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int t = __shfl_up_sync(WSW_FULL_MASK, incl, o);
@@ -271,15 +302,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane >= o) { incl += t; iincl += it; }
             }
             if (e < E) {
-                S.off[e] = run + incl - c;
-                S.ibase[e] = irun + iincl - items;
+                off[e] = run + incl - span;
+                if (blockIdx.x == 0) {
+                    hdr[1 + e] = c;
+                    hdr[1 + E + e] = run + incl - span;
+                    hdr[1 + 2 * E + e] = irun + iincl - items;
+                }
             }
             run += __shfl_sync(WSW_FULL_MASK, incl, 31);
             irun += __shfl_sync(WSW_FULL_MASK, iincl, 31);
         }
-        if (lane == 0) {
-            S.ibase[E] = irun;
-            S.nitems = irun;
+        if (blockIdx.x == 0 && lane == 0) {
+            hdr[0] = irun;
+            hdr[1 + 3 * E] = irun;
         }
     }
     __syncthreads();
@@ -287,12 +322,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = base + lane;
         const int e = m < r1 ? ids_s[m] : -1;
         const unsigned peers = __match_any_sync(WSW_FULL_MASK, e >= 0 ? e : E + lane);
-        if (e >= 0) S.list[S.off[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u))] = static_cast<uint16_t>(m);
+        if (e >= 0) pos[m] = off[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
         __syncwarp();
         if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
         __syncwarp();
     }
-    __syncthreads();  // the raw ring is free again
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int m = threadIdx.x; m < R; m += kPrepThreads)
+            if (ids_s[m] >= 0) list[pos[m]] = static_cast<int16_t>(m);
+        for (int e = threadIdx.x; e < E; e += kPrepThreads)
+            for (int p = off[e] + cnt[e]; p < off[e] + ((cnt[e] + 3) & ~3); ++p) list[p] = -1;
+    }
+    // this CTA's share of the routed rows: fp16 values (16 per thread and pass) and scales
+    const int m0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * R / gridDim.x);
+    const int m1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * R / gridDim.x);
+    // (row, 16-value chunk) pairs spread over the threads, four loads in flight each
+    const int64_t chunks = a.K / 16;
+    const int64_t work = static_cast<int64_t>(m1 - m0) * chunks;
+    for (int64_t w0 = threadIdx.x; w0 < work; w0 += 4 * kPrepThreads) {
+        uint4 v[4];
+        int64_t at[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t w = w0 + u * kPrepThreads;
+            const int m = m0 + static_cast<int>(w / chunks);
+            at[u] = -1;
+            if (w < work && ids_s[m] >= 0) {
+                const int64_t c = w - (w / chunks) * chunks;
+                v[u] = __ldg(reinterpret_cast<const uint4 *>(a.xq + static_cast<int64_t>(m) * a.K) + c);
+                at[u] = static_cast<int64_t>(pos[m]) * a.K + 16 * c;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (at[u] < 0) continue;
+            uint32_t h[8];
+            i8x16_to_h(v[u], h);
+            uint4 *dst = reinterpret_cast<uint4 *>(xh + at[u]);
+            dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+    }
+    const int64_t swork = static_cast<int64_t>(m1 - m0) * nb;
+    for (int64_t w = threadIdx.x; w < swork; w += kPrepThreads) {
+        const int m = m0 + static_cast<int>(w / nb);
+        const int b = static_cast<int>(w - (w / nb) * nb);
+        if (ids_s[m] >= 0)
+            xs[static_cast<int64_t>(b) * L.Rp + pos[m]] = __half2float(__ushort_as_half(a.xd[static_cast<int64_t>(m) * nb + b]));
+    }
+}
+
+// ---------------------------------------------------------------- main kernel --
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_q8_tc_kernel(const __grid_constant__ CUtensorMap tmWq, const __grid_constant__ CUtensorMap tmXh,
+                     const __grid_constant__ CUtensorMap tmXs, const MoeTcArgs a, const WsLayout L) {
+    extern __shared__ unsigned char smem_raw[];
+    Smem &S = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int E = static_cast<int>(a.E);
+    const int nb = static_cast<int>(a.K / 32);       // blocks per row
+    const int kst = static_cast<int>(a.K / kStageK); // stages per item
+    const uint32_t xs_bytes = static_cast<uint32_t>(nb) * kNT * 4;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRaw; ++i) { mbar_init(&S.raw_full[i], 1); mbar_init(&S.raw_empty[i], 128); }
+        for (int i = 0; i < kAB; ++i) { mbar_init(&S.a_full[i], 128); mbar_init(&S.a_empty[i], 1); }
+        for (int i = 0; i < kBS; ++i) { mbar_init(&S.b_full[i], 1); mbar_init(&S.b_empty[i], 1); }
+        for (int i = 0; i < kDStageBars; ++i) mbar_init(&S.d_full[i], 1);
+        for (int i = 0; i < kDPairs; ++i) mbar_init(&S.d_empty[i], 8);
+        // s_full: the 32 Wd-copy lanes plus the scale tile's transaction bytes
+        for (int i = 0; i < 2; ++i) { mbar_init(&S.s_full[i], 33); mbar_init(&S.s_empty[i], 256); }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    pdl_wait();  // the workspace comes from the prepass
+    const unsigned char *ws = static_cast<const unsigned char *>(a.ws);
+    const int *hdr = reinterpret_cast<const int *>(ws + L.hdr);
+    const int16_t *glist = reinterpret_cast<const int16_t *>(ws + L.list);
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        S.cnt[e] = hdr[1 + e];
+        S.off[e] = hdr[1 + E + e];
+        S.ibase[e] = hdr[1 + 2 * E + e];
+    }
+    // the list in 16-byte pieces (the workspace section is padded to 256 bytes)
+    for (int64_t q = threadIdx.x; q < (L.Rp + 7) / 8; q += kThreads)
+        reinterpret_cast<uint4 *>(S.list)[q] = __ldg(reinterpret_cast<const uint4 *>(glist) + q);
+    if (threadIdx.x == 0) {
+        S.ibase[E] = hdr[1 + 3 * E];
+        S.nitems = hdr[0];
+    }
+    __syncthreads();
     pdl_launch_dependents();
     const int NI = S.nitems;
     const int C = static_cast<int>(gridDim.x);
@@ -313,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ecur = 0;
 
     if (warp == 0) {
-        // ---------------------------------------------------------- TMA producer
+        // ---------------------------------------------------------- TMA: weights
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmWq)) : "memory");
             uint64_t pol_first, pol_last;
@@ -341,33 +461,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < my_items && ok; ++k) {
                 Item it;
                 decode_item(S, static_cast<int>(blockIdx.x) + k * C, ecur, it);
-                const uint32_t idesc = instr_desc(kRows, cols_of(it.n), false);
+                const uint32_t idesc = instr_desc(kRows, (it.n + 15) & ~15, false);
                 for (int s = 0; s < kst && ok; ++s) {
-                    const int g = k * kst + s, v = g % kAB;
-                    const uint32_t ph = (g / kAB) & 1u;
-                    if (!mbar_wait(&S.a_full[v], ph) || !mbar_wait(&S.b_full[v], ph)) {
+                    // A full also means this stage's B tile has landed (the A converters
+                    // wait for it), and the epilogue frees accumulator pairs in order, so
+                    // one wait each covers the stage
+                    const int g = k * kst + s, v = g % kAB, u = g % kBS, gp1 = 2 * g + 1;
+                    if (!mbar_wait(&S.a_full[v], (g / kAB) & 1u) ||
+                        !mbar_wait(&S.d_empty[gp1 % kDPairs], ((gp1 / kDPairs) & 1u) ^ 1u)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t bd = sw128_desc(saddr(S.bt[v]));
-                    for (int pp = 0; pp < 2; ++pp) {
-                        const int gp = 2 * g + pp, p = gp % kDPairs;
-                        if (!mbar_wait(&S.d_empty[p], ((gp / kDPairs) & 1u) ^ 1u)) { ok = false; break; }
-                        tc_fence_after();
+                    const uint64_t bd = sw128_desc(saddr(S.bt[u]));
+                    const uint32_t at0 = tmem + kACol + static_cast<uint32_t>(64 * v);
 #pragma unroll
-                        for (int jj = 0; jj < 2; ++jj) {
-                            const int j = 2 * pp + jj;  // block of the stage
-                            const uint32_t d = tmem + kDCol + static_cast<uint32_t>(128 * p + 64 * jj);
-                            const uint32_t at = tmem + kACol + static_cast<uint32_t>(64 * v + 16 * j);
-                            // block j: atom j / 2 of the B tile, bytes 64 (j % 2) + {0, 32} of its rows
-                            const uint64_t b0 = bd + static_cast<uint64_t>((j >> 1) * (kBAtom >> 4) + (j & 1) * 4);
-                            mma_ts(d, at, b0, idesc, 0u);
-                            mma_ts(d, at + 8, b0 + 2, idesc, 1u);
-                        }
-                        mma_commit(&S.d_full[p]);
+                    for (int j = 0; j < 4; ++j) {  // block j of the stage: pair 2 g + j / 2, slot half j % 2
+                        const uint32_t d = tmem + kDCol + static_cast<uint32_t>(128 * ((2 * g + (j >> 1)) % kDPairs) + 64 * (j & 1));
+                        // atom j / 2 of the B tile, bytes 64 (j % 2) + {0, 32} of its rows
+                        const uint64_t b0 = bd + static_cast<uint64_t>((j >> 1) * (kBAtom >> 4) + (j & 1) * 4);
+                        mma_ts(d, at0 + 16 * j, b0, idesc, 0u);
+                        mma_ts(d, at0 + 16 * j + 8, b0 + 2, idesc, 1u);
                     }
-                    mma_commit(&S.ab_empty[v]);
+                    mma_commit(&S.d_full[g % kDStageBars]);
+                    mma_commit(&S.a_empty[v]);
+                    mma_commit(&S.b_empty[u]);
                 }
             }
         }
@@ -384,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint4 raw[8];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4 *>(S.raw[r] + sw_off(row, c));
-                if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.ab_empty[v], ((g / kAB) & 1u) ^ 1u))) { ok = false; break; }
+                if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.a_empty[v], ((g / kAB) & 1u) ^ 1u))) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -399,135 +517,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&S.raw_empty[r]);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
+                if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.b_full[g % kBS], (g / kBS) & 1u))) { ok = false; break; }
                 mbar_arrive(&S.a_full[v]);
             }
         }
-    } else if (warp <= 7) {
-        // ---------------------------------------------------------- B converters
-        const int tt = threadIdx.x - 6 * 32;  // 0..63: B row = accumulator column
-        const int tk = tok_of(tt);            // routed row of the item in this column, or -1
-        // The correction rows (constant 1152) are written once into both B slots.
-        if (tk < 0) {
-            const uint32_t c1152 = 0x64806480u;
-#pragma unroll
-            for (int v = 0; v < kAB; ++v)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        *reinterpret_cast<uint4 *>(S.bt[v] + h * kBAtom + sw_off(tt, i)) =
-                            make_uint4(c1152, c1152, c1152, c1152);
-            fence_async_shared();
-        }
-        const int total = my_items * kst;
-        const int pieces = nb / 8;            // 16-byte pieces of a scale row
-        int kc = -1;  // item whose token row `xrow` describes
-        Item cit;
-        int ec2 = 0, ec3 = 0;
-        const int8_t *xrow = nullptr;
-        bool xzero = false;  // row inside the MMA's N but past the routed rows: zeros
-        // the 128 activation values of token tt for global stage i -> xraw[i % kXAhead]
-        auto copy_x = [&](int i) {
-            if (i < total) {
-                const int k = i / kst, s = i - k * kst;
-                if (k != kc) {
-                    decode_item(S, static_cast<int>(blockIdx.x) + k * C, ec2, cit);
-                    kc = k;
-                    xrow = tk >= 0 && tk < cit.n ? a.xq + static_cast<int64_t>(S.list[cit.tok0 + tk]) * a.K : nullptr;
-                    xzero = tk >= cit.n && tt < cols_of(cit.n);
-                }
-                if (xrow || xzero) {
-                    const int8_t *src = xrow ? xrow + s * kStageK : a.xq;
-                    const uint32_t n = xrow ? 16u : 0u;
-                    const uint32_t dst = saddr(S.xraw[i % kXAhead] + tt * kStageK);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + ((j ^ (tt & 7)) << 4)),
-                                     "l"(src + 16 * j), "r"(n)
-                                     : "memory");
+    } else if (warp == 6) {
+        // ---------------------------------------------------------- TMA: activations
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmXh)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmXs)) : "memory");
+            uint64_t pol;
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+            for (int k = 0; k < my_items && ok; ++k) {
+                Item it;
+                decode_item(S, static_cast<int>(blockIdx.x) + k * C, ecur, it);
+                const int sb = k & 1;
+                // the item's activation scales: fp32 [block][64 sorted rows] (x = tok0, a
+                // multiple of 4, so the copy starts on a 16-byte boundary)
+                if (!mbar_wait(&S.s_empty[sb], ((k >> 1) & 1u) ^ 1u)) { ok = false; break; }
+                mbar_expect_tx(&S.s_full[sb], xs_bytes);
+                tma_load_2d(&S.xs[sb][0][0], &tmXs, it.tok0, 0, &S.s_full[sb], pol);
+                for (int s = 0; s < kst; ++s) {
+                    const int g = k * kst + s, u = g % kBS;
+                    if (!mbar_wait(&S.b_empty[u], ((g / kBS) & 1u) ^ 1u)) { ok = false; break; }
+                    mbar_expect_tx(&S.b_full[u], kBBytes);
+                    tma_load_2d(S.bt[u], &tmXh, s * kStageK, it.tok0, &S.b_full[u], pol);
+                    tma_load_2d(S.bt[u] + kBAtom, &tmXh, s * kStageK + 64, it.tok0, &S.b_full[u], pol);
                 }
             }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        };
-        // the scale rows of item kk (128 Wd rows into wd[kk % 2], this thread's xd row into
-        // xdr) join the cp.async group committed next; buffer kk % 2 must be released by
-        // the epilogue of item kk - 2 first
-        auto copy_scales = [&](int kk) -> bool {
-            if (kk >= my_items) return true;
-            Item si;
-            decode_item(S, static_cast<int>(blockIdx.x) + kk * C, ec3, si);
-            if (!mbar_wait(&S.s_empty[kk & 1], ((kk >> 1) & 1u) ^ 1u)) return false;
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const int r = tt + 64 * rr;
-                const int64_t o = si.m0 + r;
+        }
+        __syncwarp();
+    } else if (warp == 7) {
+        // ---------------------------------------------------------- Wd rows of each item
+        const int pieces = nb / 8;  // 16-byte pieces of a scale row
+        for (int k = 0; k < my_items && ok; ++k) {
+            Item it;
+            decode_item(S, static_cast<int>(blockIdx.x) + k * C, ecur, it);
+            const int sb = k & 1;
+            if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.s_empty[sb], ((k >> 1) & 1u) ^ 1u))) { ok = false; break; }
+#pragma unroll 1
+            for (int rr = 0; rr < 4; ++rr) {
+                const int r = lane + 32 * rr;
+                const int64_t o = it.m0 + r;
                 const bool valid = o < a.Mo;
-                const uint16_t *src = a.Wd + (si.e * a.Mo + (valid ? o : 0)) * nb;
-                const uint32_t dst = saddr(S.wd[kk & 1] + r * kScalePitch);
+                const uint16_t *src = a.Wd + (it.e * a.Mo + (valid ? o : 0)) * nb;
+                const uint32_t dst = saddr(S.wd[sb] + r * kScalePitch);
                 for (int p = 0; p < pieces; ++p)
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + 16 * p), "l"(src + 8 * p),
                                  "r"(valid ? 16u : 0u)
                                  : "memory");
             }
-            const bool valid = tk >= 0 && tk < si.n;
-            const uint16_t *src = a.xd + static_cast<int64_t>(valid ? S.list[si.tok0 + tk] : 0) * nb;
-            const uint32_t dst = saddr(S.xdr + tt * kScalePitch);
-            for (int p = 0; p < pieces; ++p)
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + 16 * p), "l"(src + 8 * p),
-                             "r"(valid ? 16u : 0u)
-                             : "memory");
-            return true;
-        };
-        if (!copy_scales(0)) ok = false;
-        for (int i = 0; i < kXAhead - 1; ++i) copy_x(i);
-        for (int k = 0; k < my_items && ok; ++k) {
-            Item it;
-            decode_item(S, static_cast<int>(blockIdx.x) + k * C, ecur, it);
-            const int N = cols_of(it.n);
-            for (int s = 0; s < kst; ++s) {
-                const int g = k * kst + s, v = g % kAB;
-                if (s == kst / 2 && !copy_scales(k + 1)) { ok = false; break; }
-                copy_x(g + kXAhead - 1);
-                asm volatile("cp.async.wait_group %0;" ::"n"(kXAhead - 1) : "memory");
-                if (s == 0) {
-                    // this item's scale rows have landed: xd -> fp32 [block][token]
-                    const unsigned char *xr = S.xdr + tt * kScalePitch;
-                    for (int p = 0; p < pieces; ++p) {
-                        const uint4 v4 = *reinterpret_cast<const uint4 *>(xr + 16 * p);
-                        const __half *h = reinterpret_cast<const __half *>(&v4);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) S.xs[k & 1][8 * p + i][tt] = __half2float(h[i]);
-                    }
-                    mbar_arrive(&S.s_full[k & 1]);
-                }
-                const unsigned char *xr = S.xraw[g % kXAhead] + tt * kStageK;
-                if (!mbar_wait(&S.ab_empty[v], ((g / kAB) & 1u) ^ 1u)) { ok = false; break; }
-                if (tt < N && tk >= 0) {
-                    // values 64 h .. 64 h + 63 of the stage = atom h of the B tile
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t w[32];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            i8x16_to_h_biased(*reinterpret_cast<const uint4 *>(xr + (((4 * h + j) ^ (tt & 7)) << 4)), &w[8 * j]);
-                        unsigned char *B = S.bt[v] + h * kBAtom;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            *reinterpret_cast<uint4 *>(B + sw_off(tt, i)) =
-                                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                    }
-                    fence_async_shared();
-                }
-                mbar_arrive(&S.b_full[v]);
-            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            mbar_arrive(&S.s_full[sb]);
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
         // ---------------------------------------------------------- epilogue
-        // Two groups of four warps (one per lane quarter).  Items with at most 32 routed
-        // rows: group h takes the blocks of parity h (32 columns each) and group 1 hands
-        // its sums to group 0; items with more: group h takes every block, columns
-        // 32 h .. 32 h + 31.
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const int grp = (warp - 8) >> 2;
@@ -536,35 +581,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             Item it;
             decode_item(S, static_cast<int>(blockIdx.x) + k * C, ecur, it);
             const int sb = k & 1;
-            const bool split_cols = it.n > kHalf;
+            const bool split_cols = it.n > 32;
             const int c0 = split_cols ? 32 * grp : 0;  // first accumulator column of this thread
             if (ok && !__all_sync(WSW_FULL_MASK, mbar_wait(&S.s_full[sb], (k >> 1) & 1u))) ok = false;
-            float acc[kHalf];
+            uint64_t acc2[16];  // accumulators of columns c0 + 2 i, c0 + 2 i + 1
 #pragma unroll
-            for (int j = 0; j < kHalf; ++j) acc[j] = 0.0f;
-            // block b's 32 columns c0 .. c0 + 31: routed rows, then the correction 1152 * S
+            for (int i = 0; i < 16; ++i) acc2[i] = 0ull;
+            // acc += fl(Wd * xd) * isum per column: the scalar arithmetic, two columns an instruction
             auto scale_add = [&](int b, const uint32_t(&dv)[32]) {
                 const float wd = __half2float(reinterpret_cast<const __half *>(S.wd[sb] + row * kScalePitch)[b]);
-                const float wdc = wd * __uint_as_float(dv[kHalf]);
+                const uint64_t ww = f2_pack(wd, wd);
                 const float4 *xs4 = reinterpret_cast<const float4 *>(&S.xs[sb][b][c0]);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 xs = xs4[j4];
-                    const float x[4] = {xs.x, xs.y, xs.z, xs.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int j = 4 * j4 + i;
-                        if (j < kHalf)  // Wd * isum = Wd * (D - 1152 S), one rounding
-                            acc[j] = fmaf(x[i], fmaf(__uint_as_float(dv[j]), wd, -wdc), acc[j]);
-                    }
+                    f2_scale_fma(acc2[2 * j4], ww, f2_pack(xs.x, xs.y),
+                                 f2_pack(__uint_as_float(dv[4 * j4]), __uint_as_float(dv[4 * j4 + 1])));
+                    f2_scale_fma(acc2[2 * j4 + 1], ww, f2_pack(xs.z, xs.w),
+                                 f2_pack(__uint_as_float(dv[4 * j4 + 2]), __uint_as_float(dv[4 * j4 + 3])));
                 }
             };
             // pair gp = 2 g + pp holds blocks 4 s + 2 pp and 4 s + 2 pp + 1 of stage s
             for (int s = 0; s < kst && ok; ++s) {
-                for (int pp = 0; pp < 2 && ok; ++pp) {
-                    const int gp = 2 * (k * kst + s) + pp, p = gp % kDPairs;
-                    if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.d_full[p], (gp / kDPairs) & 1u))) { ok = false; break; }
-                    tc_fence_after();
+                const int g = k * kst + s;
+                if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.d_full[g % kDStageBars], (g / kDStageBars) & 1u))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int gp = 2 * g + pp, p = gp % kDPairs;
                     const uint32_t pa = lane_addr + static_cast<uint32_t>(128 * p);
                     uint32_t dv[32];
                     if (!split_cols) {
@@ -588,26 +634,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             mbar_arrive(&S.s_empty[sb]);
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f2_unpack(acc2[i], acc[2 * i], acc[2 * i + 1]);
             const int64_t o = it.m0 + row;
             const float nan = __int_as_float(0x7fc00000);
             if (split_cols) {
-                const int t0 = grp * kHalf;  // routed rows of columns c0 .. c0 + 30
                 if (o < a.Mo) {
 #pragma unroll
-                    for (int j = 0; j < kHalf; ++j)
-                        if (t0 + j < it.n)
-                            a.y[static_cast<int64_t>(S.list[it.tok0 + t0 + j]) * a.Mo + o] = ok ? acc[j] : nan;
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j < it.n)
+                            a.y[static_cast<int64_t>(S.list[it.tok0 + c0 + j]) * a.Mo + o] = ok ? acc[j] : nan;
                 }
             } else {
                 // group 1 hands its sums to group 0
                 if (grp == 1) {
 #pragma unroll
-                    for (int j = 0; j < kHalf; ++j) S.comb[j][row] = ok ? acc[j] : nan;
+                    for (int j = 0; j < 32; ++j) S.comb[j][row] = ok ? acc[j] : nan;
                 }
                 asm volatile("bar.sync 1, 256;" ::: "memory");
                 if (grp == 0 && o < a.Mo) {
 #pragma unroll
-                    for (int j = 0; j < kHalf; ++j)
+                    for (int j = 0; j < 32; ++j)
                         if (j < it.n)
                             a.y[static_cast<int64_t>(S.list[it.tok0 + j]) * a.Mo + o] =
                                 ok ? acc[j] + S.comb[j][row] : nan;
@@ -638,36 +686,63 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_moe() {
     return fn;
 }
 
+bool make_map_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t inner, uint64_t outer,
+                 uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    auto fn = encode_fn_moe();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
+size_t moe_q8_tc_workspace_bytes(int64_t E, int64_t K, int64_t R) {
+    if (E <= 0 || K <= 0 || R <= 0) return 0;
+    return ws_layout(E, K, R).bytes;
+}
+
 // Whether the tensor-core path takes this problem (the caller falls back otherwise).
-bool moe_q8_tc_supported(int64_t E, int64_t Mo, int64_t K, int64_t R, const void *Wq, const void *Wd,
-                         const void *xq, const void *xd) {
+bool moe_q8_tc_supported(const MoeTcArgs &a) {
     // K: whole 128-value stages and 16-byte pieces of a scale row (K % 256), at most
-    // kMaxBlocks blocks; the routing ids and per-warp counts fit the raw ring during
-    // bucketing; the lists fit shared memory.
-    return K % 256 == 0 && K / 32 <= kMaxBlocks && R <= kMaxList && E <= kMaxE &&
-           (R + kBucketWarps * E) * 4 <= kRaw * kRawBytes && E * Mo <= 0x7fffffffLL &&
-           ((reinterpret_cast<uintptr_t>(Wq) | reinterpret_cast<uintptr_t>(Wd) | reinterpret_cast<uintptr_t>(xq) |
-             reinterpret_cast<uintptr_t>(xd)) & 15) == 0;
+    // kMaxBlocks blocks; the routed rows, experts and sorted positions fit shared
+    // memory; a workspace of the layout's size, 256-byte aligned.
+    if (a.K % 256 != 0 || a.K / 32 > kMaxBlocks || a.R > kMaxRows || a.E > kMaxE || a.E * a.Mo > 0x7fffffffLL)
+        return false;
+    if (((reinterpret_cast<uintptr_t>(a.Wq) | reinterpret_cast<uintptr_t>(a.Wd) | reinterpret_cast<uintptr_t>(a.xq) |
+          reinterpret_cast<uintptr_t>(a.xd)) & 15) != 0)
+        return false;
+    return a.ws != nullptr && (reinterpret_cast<uintptr_t>(a.ws) & 255) == 0 &&
+           a.ws_bytes >= ws_layout(a.E, a.K, a.R).bytes;
 }
 
 int moe_q8_tc_launch(const MoeTcArgs &a, int sm_count, cudaStream_t s, bool pdl) {
-    auto fn = encode_fn_moe();
-    if (!fn) return WSW_ERR_CUDA;
-    CUtensorMap map;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.E * a.Mo)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K)};
-    cuuint32_t box[2] = {kStageK, kRows};
-    cuuint32_t estr[2] = {1, 1};
-    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(a.Wq), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    const WsLayout L = ws_layout(a.E, a.K, a.R);
+    unsigned char *ws = static_cast<unsigned char *>(a.ws);
+    CUtensorMap mW, mXh, mXs;
+    if (!make_map_2d(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, a.K, a.E * a.Mo, a.K, kStageK, kRows,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&mXh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws + L.xh, a.K, L.Rp, a.K * 2, 64, kNT,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&mXs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws + L.xs, L.Rp, a.K / 32, L.Rp * 4, kNT,
+                     static_cast<uint32_t>(a.K / 32), CU_TENSOR_MAP_SWIZZLE_NONE))
         return WSW_ERR_CUDA;
-    const size_t smem = sizeof(Smem) + 1024;
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(moe_q8_tc_kernel), static_cast<int>(smem));
+    // the prepass: one CTA per SM (at most one per routed row)
+    const size_t prep_smem = static_cast<size_t>(2 * a.R + (kBucketWarps + 2) * a.E) * 4;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(moe_q8_prep_kernel), static_cast<int>(prep_smem));
     if (e != cudaSuccess) return WSW_ERR_CUDA;
-    e = launch(moe_q8_tc_kernel, dim3(static_cast<unsigned>(sm_count)), dim3(kThreads), smem, s, pdl, map, a);
+    const unsigned prep_ctas = static_cast<unsigned>(a.R < sm_count ? a.R : sm_count);
+    e = launch(moe_q8_prep_kernel, dim3(prep_ctas), dim3(kPrepThreads), prep_smem, s, pdl, a, L);
+    if (e != cudaSuccess) return WSW_ERR_CUDA;
+    // the product, programmatically dependent on the prepass
+    const size_t smem = sizeof(Smem) + 1024;
+    e = ensure_smem(reinterpret_cast<const void *>(moe_q8_tc_kernel), static_cast<int>(smem));
+    if (e != cudaSuccess) return WSW_ERR_CUDA;
+    e = launch(moe_q8_tc_kernel, dim3(static_cast<unsigned>(sm_count)), dim3(kThreads), smem, s, true, mW, mXh, mXs,
+               a, L);
     return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
 }
 

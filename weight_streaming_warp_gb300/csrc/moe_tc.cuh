@@ -20,13 +20,17 @@ struct MoeTcArgs {
     int64_t R;
     float *y;
     int32_t *err;
+    void *ws;         // caller workspace (the prepass's sorted activations), or NULL
+    size_t ws_bytes;
 };
 
-// Whether the tensor-core path can take this problem.
-bool moe_q8_tc_supported(int64_t E, int64_t Mo, int64_t K, int64_t R, const void *Wq, const void *Wd,
-                         const void *xq, const void *xd);
+// Workspace bytes of the tensor-core form for these sizes.
+size_t moe_q8_tc_workspace_bytes(int64_t E, int64_t K, int64_t R);
 
-// Launch it (one persistent CTA per SM); returns a wsw_status.
+// Whether the tensor-core path can take this problem (it needs the workspace).
+bool moe_q8_tc_supported(const MoeTcArgs &a);
+
+// Launch it (a prepass, then one persistent CTA per SM); returns a wsw_status.
 int moe_q8_tc_launch(const MoeTcArgs &a, int sm_count, cudaStream_t s, bool pdl);
 
 // The form for a few routed rows (gemv_q8_0.cu): a dense mat-vec over R * Mo gathered
