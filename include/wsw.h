@@ -219,6 +219,33 @@ int wsw_moe_gemv_q8_0(const int8_t *Wq, const uint16_t *Wd, int64_t E, int64_t M
                       const wsw_launch_opts *opts);
 
 /*
+ * wsw_moe_gemv_q8_0_noalloc -- wsw_moe_gemv_q8_0 for callers that cannot allocate device
+ * memory, such as a plugin or custom-operator interface that receives only its input
+ * and output buffers, a runtime that reserves all device memory in its own pool at
+ * start-up, or a path that cannot accept cudaMalloc's device synchronisation.  The pages
+ * have no counterpart: this is a convenience of this library.
+ *
+ * Arguments, results and errors are those of wsw_moe_gemv_q8_0, except that there is
+ * no ws / ws_bytes.  The workspace is a fixed 8 MiB scratch array inside the library,
+ * which every GPU that loads the library holds until the process exits.  Sizes whose
+ * wsw_moe_workspace_bytes(E, K, R) exceeds 8 MiB return WSW_ERR_UNSUPPORTED and launch
+ * nothing (for example E = 128 takes R up to 1540 routed rows at K = 2048, and up to
+ * 4096 at K = 768, the tensor-core limit).  The call
+ * performs no cudaMalloc, cudaFree or other allocation.
+ *
+ *   - The first call on a device looks up the scratch array's device address on that
+ *     device (it must be the current device).  Make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one scratch array and leaves its contents
+ *     behind.  Nothing in it needs to start at zero, because each call writes what it
+ *     reads.  Calls whose executions overlap on the GPU (for example on two streams)
+ *     race on the scratch; calls on one stream do not.
+ */
+int wsw_moe_gemv_q8_0_noalloc(const int8_t *Wq, const uint16_t *Wd, int64_t E, int64_t Mo, int64_t K,
+                              const int8_t *xq, const uint16_t *xd, const int32_t *ids, int64_t R,
+                              float *y, int32_t *err_flag, void *stream, const wsw_launch_opts *opts);
+
+/*
  * wsw_dequant_q8_0_kv -- dequantize one layer's q8_0 K (or V) cache once into a
  * per-head-contiguous binary16 buffer ([P1] Overview and the stride discussion:
  * the cache walks [dim][position][head] with a position stride of
