@@ -220,7 +220,7 @@ __device__ __forceinline__ void decode_item(const Smem &S, int i, int &ecur, Ite
 // Every CTA buckets the ids (the same stable lists everywhere), CTA 0 writes the header
 // and the sorted-position list, and every CTA converts its share of the routed rows.
 // Dynamic shared memory: ids[R], wcnt[kBucketWarps][E], cnt[E], off[E], pos[R] (ints).
-__global__ void __launch_bounds__(kPrepThreads) moe_q8_prep_kernel(const MoeTcArgs a, const WsLayout L) {
+__global__ void __launch_bounds__(kPrepThreads, 1) moe_q8_prep_kernel(const MoeTcArgs a, const WsLayout L) {
     extern __shared__ int prep_smem[];
     const int E = static_cast<int>(a.E);
     const int R = static_cast<int>(a.R);
@@ -263,6 +263,29 @@ __global__ void __launch_bounds__(kPrepThreads) moe_q8_prep_kernel(const MoeTcAr
         }
         if (bad && blockIdx.x == 0 && a.err) atomicOr(a.err, 1);
         for (int i = threadIdx.x; i < kBucketWarps * E; i += kPrepThreads) wcnt[i] = 0;
+    }
+    // This CTA's share of the routed rows: the first kPre (row, 16-value chunk) pieces of
+    // each thread and its scale pieces are requested now, so that their latency hides
+    // behind the bucketing (whether a row is used is known only afterwards).
+    const int m0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * R / gridDim.x);
+    const int m1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * R / gridDim.x);
+    const int64_t chunks = a.K / 16;
+    const int64_t work = static_cast<int64_t>(m1 - m0) * chunks;
+    const int64_t swork = static_cast<int64_t>(m1 - m0) * (nb / 8);  // 8 binary16 scales a piece
+    constexpr int kPre = 8;
+    uint4 pre[kPre], spre;
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+        const int64_t w = threadIdx.x + static_cast<int64_t>(u) * kPrepThreads;
+        if (w < work) {
+            const int64_t r = w / chunks;
+            pre[u] = __ldg(reinterpret_cast<const uint4 *>(a.xq + static_cast<int64_t>(m0 + r) * a.K) + (w - r * chunks));
+        }
+    }
+    if (threadIdx.x < swork) {
+        const int64_t r = threadIdx.x / (nb / 8);
+        spre = __ldg(reinterpret_cast<const uint4 *>(a.xd + static_cast<int64_t>(m0 + r) * nb) +
+                     (threadIdx.x - r * (nb / 8)));
     }
     __syncthreads();
     const int r0 = warp < kBucketWarps ? static_cast<int>(static_cast<int64_t>(warp) * R / kBucketWarps) : 0;
@@ -334,42 +357,53 @@ __global__ void __launch_bounds__(kPrepThreads) moe_q8_prep_kernel(const MoeTcAr
         for (int e = threadIdx.x; e < E; e += kPrepThreads)
             for (int p = off[e] + cnt[e]; p < off[e] + ((cnt[e] + 3) & ~3); ++p) list[p] = -1;
     }
-    // this CTA's share of the routed rows: fp16 values (16 per thread and pass) and scales
-    const int m0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * R / gridDim.x);
-    const int m1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * R / gridDim.x);
-    // (row, 16-value chunk) pairs spread over the threads, four loads in flight each
-    const int64_t chunks = a.K / 16;
-    const int64_t work = static_cast<int64_t>(m1 - m0) * chunks;
-    for (int64_t w0 = threadIdx.x; w0 < work; w0 += 4 * kPrepThreads) {
+    // convert the preloaded pieces to fp16 at their sorted rows, then any remaining ones
+    // (four loads in flight a pass)
+    auto put = [&](int64_t w, const uint4 &v) {
+        const int64_t r = w / chunks;
+        const int m = m0 + static_cast<int>(r);
+        if (ids_s[m] < 0) return;
+        uint32_t h[8];
+        i8x16_to_h(v, h);
+        uint4 *dst = reinterpret_cast<uint4 *>(xh + static_cast<int64_t>(pos[m]) * a.K + 16 * (w - r * chunks));
+        dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+        dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    };
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+        const int64_t w = threadIdx.x + static_cast<int64_t>(u) * kPrepThreads;
+        if (w < work) put(w, pre[u]);
+    }
+    for (int64_t w0 = threadIdx.x + static_cast<int64_t>(kPre) * kPrepThreads; w0 < work; w0 += 4 * kPrepThreads) {
         uint4 v[4];
-        int64_t at[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int64_t w = w0 + u * kPrepThreads;
-            const int m = m0 + static_cast<int>(w / chunks);
-            at[u] = -1;
-            if (w < work && ids_s[m] >= 0) {
-                const int64_t c = w - (w / chunks) * chunks;
-                v[u] = __ldg(reinterpret_cast<const uint4 *>(a.xq + static_cast<int64_t>(m) * a.K) + c);
-                at[u] = static_cast<int64_t>(pos[m]) * a.K + 16 * c;
+            if (w < work) {
+                const int64_t r = w / chunks;
+                v[u] = __ldg(reinterpret_cast<const uint4 *>(a.xq + static_cast<int64_t>(m0 + r) * a.K) + (w - r * chunks));
             }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            if (at[u] < 0) continue;
-            uint32_t h[8];
-            i8x16_to_h(v[u], h);
-            uint4 *dst = reinterpret_cast<uint4 *>(xh + at[u]);
-            dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-            dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+            const int64_t w = w0 + u * kPrepThreads;
+            if (w < work) put(w, v[u]);
         }
     }
-    const int64_t swork = static_cast<int64_t>(m1 - m0) * nb;
-    for (int64_t w = threadIdx.x; w < swork; w += kPrepThreads) {
-        const int m = m0 + static_cast<int>(w / nb);
-        const int b = static_cast<int>(w - (w / nb) * nb);
-        if (ids_s[m] >= 0)
-            xs[static_cast<int64_t>(b) * L.Rp + pos[m]] = __half2float(__ushort_as_half(a.xd[static_cast<int64_t>(m) * nb + b]));
+    // scales: 8 per piece, fp32 at [block][sorted row]
+    auto put_scales = [&](int64_t w, const uint4 &v) {
+        const int64_t r = w / (nb / 8);
+        const int m = m0 + static_cast<int>(r);
+        if (ids_s[m] < 0) return;
+        const int b0 = 8 * static_cast<int>(w - r * (nb / 8));
+        const __half *hv = reinterpret_cast<const __half *>(&v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xs[static_cast<int64_t>(b0 + i) * L.Rp + pos[m]] = __half2float(hv[i]);
+    };
+    if (threadIdx.x < swork) put_scales(threadIdx.x, spre);
+    for (int64_t w = threadIdx.x + kPrepThreads; w < swork; w += kPrepThreads) {
+        const int64_t r = w / (nb / 8);
+        put_scales(w, __ldg(reinterpret_cast<const uint4 *>(a.xd + static_cast<int64_t>(m0 + r) * nb) + (w - r * (nb / 8))));
     }
 }
 
