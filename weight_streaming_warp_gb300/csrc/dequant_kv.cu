@@ -12,8 +12,8 @@
 // The fp32 product is exact (11 x 8 significant bits); __float2half_rn rounds once.
 //
 // Each thread converts 16 values (one 16-byte load, two 16-byte stores); a CTA covers
-// 4 x 256 consecutive 16-value pieces of the input, all loads issued before the first
-// conversion.  Reads are sequential in input order; each group of head_dim/16 threads
+// 4 x 256 consecutive 16-value pieces of the input, requested into L2 before the
+// dependency wait and loaded before the first conversion.  Reads are sequential in input order; each group of head_dim/16 threads
 // writes one contiguous output row.
 #include <cuda_fp16.h>
 
@@ -30,6 +30,15 @@ __global__ void __launch_bounds__(kThreads) dequant_q8_0_kv_kernel(
     const int8_t *__restrict__ q, const uint16_t *__restrict__ d, int64_t depth, int64_t heads,
     int64_t head_dim, uint16_t *__restrict__ out, int64_t npieces) {
     pdl_launch_dependents();
+    // This CTA's input lines are requested into L2 before the dependency wait: L2 is the
+    // point of coherence, so lines an earlier kernel is still writing (the newly appended
+    // positions) are read correctly after the wait, and the rest arrive early.
+    {
+        const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kPieces * kThreads;
+        const int64_t p1 = p0 + kPieces * kThreads < npieces ? p0 + kPieces * kThreads : npieces;
+        prefetch_range_l2(q + 16 * p0, 16 * (p1 - p0));
+        prefetch_range_l2(d + p0 / 2, (p1 - p0));  // one binary16 scale per two pieces
+    }
     pdl_wait();  // the cache is written by earlier kernels
     const int64_t per_pos = heads * head_dim / 16;  // pieces per position
     const int64_t per_head = head_dim / 16;         // pieces per head row
