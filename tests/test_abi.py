@@ -99,6 +99,7 @@ def test_other_calls_reject_on_host(lib):
     assert m(P(4096), P(4096), 8, 16, 64, P(4096), P(4096), P(4096), 0, P(4096), None, None, 0, None, None) == 0
     w = lib.wsw_moe_workspace_bytes
     assert w(128, 2048, 16) == 0 and w(128, 2048, 256) == 0 and w(128, 96, 4096) == 0
+    assert w(128, 2048, 4097) == 0 and w(513, 2048, 1024) == 0 and w(8, 4096, 1024) == 0  # CUDA-core sizes
     # sorted positions (R + 3 per used expert, rounded to 4): fp16 rows, fp32 scales, list, header
     n = w(128, 2048, 4096)
     rp = 4096 + 3 * 128

@@ -364,7 +364,7 @@ cudaError_t launch_cc(bool split, const MoeArgs &a, unsigned ctas, size_t smem, 
 }  // namespace wsw
 
 extern "C" size_t wsw_moe_workspace_bytes(int64_t E, int64_t K, int64_t R) {
-    if (R <= wsw::kTcMinRows || K % 256 != 0) return 0;
+    if (R <= wsw::kTcMinRows) return 0;
     return wsw::moe_q8_tc_workspace_bytes(E, K, R);
 }
 

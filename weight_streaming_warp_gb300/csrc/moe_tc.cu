@@ -734,18 +734,21 @@ bool make_map_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, u
 
 }  // namespace
 
+// Sizes the tensor-core form takes: whole 128-value stages and 16-byte pieces of a scale
+// row (K % 256), at most kMaxBlocks blocks; routed rows, experts and sorted positions
+// that fit shared memory.
+static bool tc_shape_ok(int64_t E, int64_t K, int64_t R) {
+    return E > 0 && K > 0 && R > 0 && K % 256 == 0 && K / 32 <= kMaxBlocks && R <= kMaxRows && E <= kMaxE;
+}
+
 size_t moe_q8_tc_workspace_bytes(int64_t E, int64_t K, int64_t R) {
-    if (E <= 0 || K <= 0 || R <= 0) return 0;
-    return ws_layout(E, K, R).bytes;
+    return tc_shape_ok(E, K, R) ? ws_layout(E, K, R).bytes : 0;
 }
 
 // Whether the tensor-core path takes this problem (the caller falls back otherwise).
 bool moe_q8_tc_supported(const MoeTcArgs &a) {
-    // K: whole 128-value stages and 16-byte pieces of a scale row (K % 256), at most
-    // kMaxBlocks blocks; the routed rows, experts and sorted positions fit shared
-    // memory; a workspace of the layout's size, 256-byte aligned.
-    if (a.K % 256 != 0 || a.K / 32 > kMaxBlocks || a.R > kMaxRows || a.E > kMaxE || a.E * a.Mo > 0x7fffffffLL)
-        return false;
+    // the sizes above, and a workspace of the layout's size, 256-byte aligned
+    if (!tc_shape_ok(a.E, a.K, a.R) || a.E * a.Mo > 0x7fffffffLL) return false;
     if (((reinterpret_cast<uintptr_t>(a.Wq) | reinterpret_cast<uintptr_t>(a.Wd) | reinterpret_cast<uintptr_t>(a.xq) |
           reinterpret_cast<uintptr_t>(a.xd)) & 15) != 0)
         return false;
