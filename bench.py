@@ -73,6 +73,19 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def whole_job_rate(pg, torch, elapsed_s, units_per_rank, device="cpu"):
+    """Whole-job rate over the ranks of process group pg (None: one process): the
+    slowest rank's elapsed time (max over ranks) and the units of all ranks, so
+    value = units_per_rank * world / max_elapsed.  Returns (value, max_elapsed)."""
+    world = 1
+    if pg is not None:
+        world = pg.get_world_size()
+        t = torch.tensor([elapsed_s], device=device, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_s = float(t.item())
+    return units_per_rank * world / elapsed_s, elapsed_s
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -563,13 +576,9 @@ def run_ours(args):
         pg.barrier()
     clocks.mark(t0, t1)
     clk = clocks.stop()
-    elapsed = e0.elapsed_time(e1) / 1000.0
-    if pg:
-        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        elapsed = float(tt.item())
+    value, elapsed = whole_job_rate(pg, torch, e0.elapsed_time(e1) / 1000.0,
+                                    B_TOKEN * TOKENS * args.steps / 1e9, device=dev)
     step_s = elapsed / args.steps
-    value = B_TOKEN * TOKENS * world / step_s / 1e9
 
     # the same step with the quantizer as its own launch
     two_graph = _graph(torch, lambda stream: wl.step(stream, fused=False))
