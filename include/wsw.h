@@ -66,7 +66,8 @@ typedef enum wsw_status {
 typedef struct wsw_launch_opts {
     int32_t rows_per_warp; /* output rows one warp reduces together: 1, 2 or 4
                               (the pages' rows per workgroup, [P4] "What did NOT
-                              work"); 0 = 2 */
+                              work"); 0 = the library's choice (2; 4 for bf16
+                              mat-vecs of at least 16384 rows) */
     int32_t load_bytes;    /* cap on the weight load width: 32, 16, 8, 4 or 2;
                               0 = 32 (one 256-bit load per lane) */
     int32_t pdl;           /* 1 = launch with programmatic dependent launch: the

