@@ -242,6 +242,8 @@ struct Q8G : Q8 {
         else Q8::zero(b);
     }
     __device__ __forceinline__ static void prefetch_x(const Args &) {}
+    // All R activations in one pass over (routed row, 16-byte piece) pairs, four loads in
+    // flight per thread before their stores, in Q8's layout per routed row.
     template <bool XS>
     __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
         if (threadIdx.x < a.R) {
@@ -250,11 +252,63 @@ struct Q8G : Q8 {
             ids_smem()[threadIdx.x] = ok ? e : -1;
             if (!ok && blockIdx.x == 0 && a.err) atomicOr(a.err, 1);
         }
-        for (int64_t m = 0; m < a.R; ++m) {
-            Q8::Args t = a;
-            t.xq = a.xq + m * a.K;
-            t.xd = a.xd + m * (a.K / 32);
-            Q8::stage_x<XS>(t, xsm + m * token_bytes(nsteps), nsteps);
+        const int64_t nslots = static_cast<int64_t>(nsteps) * 32;
+        const int64_t tb = token_bytes(nsteps);
+        const int64_t nblk = a.K / 32;
+        const bool xvec = (reinterpret_cast<uintptr_t>(a.xq) & 15) == 0;
+        const int64_t nh = 2 * nslots;  // 16-byte halves of one routed row (padded past K)
+        const int64_t total = a.R * nh;
+        for (int64_t i0 = threadIdx.x; i0 < total; i0 += 4 * static_cast<int64_t>(blockDim.x)) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * static_cast<int64_t>(blockDim.x);
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < total) {
+                    const int64_t m = i / nh, h = i - m * nh;
+                    const int8_t *row = a.xq + m * a.K;
+                    if (16 * h < a.K) {
+                        if (xvec) {
+                            v[u] = __ldg(reinterpret_cast<const uint4 *>(row) + h);
+                        } else {
+                            uint32_t t[4] = {0u, 0u, 0u, 0u};
+                            for (int j = 0; j < 16; ++j)
+                                t[j >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(row[16 * h + j])) << (8 * (j & 3));
+                            v[u] = make_uint4(t[0], t[1], t[2], t[3]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * static_cast<int64_t>(blockDim.x);
+                if (i < total) {
+                    const int64_t m = i / nh, h = i - m * nh;
+                    // half h = bytes 16h .. 16h+15 = plane (h & 1) of block h >> 1
+                    reinterpret_cast<uint4 *>(xsm + m * tb)[(h & 1) * nslots + (h >> 1)] = v[u];
+                }
+            }
+        }
+        const int64_t dtotal = a.R * nslots;
+        for (int64_t i0 = threadIdx.x; i0 < dtotal; i0 += 4 * static_cast<int64_t>(blockDim.x)) {
+            uint16_t dv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * static_cast<int64_t>(blockDim.x);
+                dv[u] = 0;
+                if (i < dtotal) {
+                    const int64_t m = i / nslots, b = i - m * nslots;
+                    if (b < nblk) dv[u] = a.xd[m * nblk + b];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * static_cast<int64_t>(blockDim.x);
+                if (i < dtotal) {
+                    const int64_t m = i / nslots, b = i - m * nslots;
+                    reinterpret_cast<uint16_t *>(xsm + m * tb + 32 * nslots)[b] = dv[u];
+                }
+            }
         }
     }
     template <bool XS>
