@@ -35,7 +35,7 @@
  *     the weight load width degrades 32 -> 16 -> 8 -> 4 -> 2 bytes until aligned,
  *     and the result is bit-identical to the 32-byte path ([P4] "What shipped": the
  *     load width degrades one step at a time when an offset is misaligned).
- *     The exception is wsw_gemm_bf16, whose tensor-memory loads need 16-byte
+ *     The exception is wsw_gemm_bf16, whose TMA tile loads need 16-byte
  *     alignment (WSW_ERR_MISALIGNED otherwise).
  *   - Results do not depend on wsw_launch_opts: any rows_per_warp, load_bytes,
  *     pdl or ctas_per_sm gives bit-identical output ([P4] "What did NOT work":
@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define WSW_ABI_VERSION 2
+#define WSW_ABI_VERSION 3
 
 typedef enum wsw_status {
     WSW_OK = 0,
@@ -59,7 +59,9 @@ typedef enum wsw_status {
     WSW_ERR_MISALIGNED = 2,  /* alignment that the call cannot degrade around */
     WSW_ERR_UNSUPPORTED = 3, /* device is not sm_103 / shape beyond a stated limit */
     WSW_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
-    WSW_ERR_TIMEOUT = 6      /* reserved for bounded device-side waits */
+    WSW_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up (read on the
+                                device: wsw_bounded_wait_check, bit 1 of the MoE
+                                error flag) */
 } wsw_status;
 
 /* Launch knobs.  Pass NULL for the defaults.  0 in a field means "choose". */
@@ -144,6 +146,37 @@ typedef struct wsw_gemv_link {
 int wsw_gemv_bf16_chain(int64_t n_links, const wsw_gemv_link *links, void *stream,
                         const wsw_launch_opts *opts);
 
+/* The launch that wsw_gemv_bf16 (or one link of wsw_gemv_bf16_chain) makes. */
+typedef struct wsw_gemv_plan {
+    int32_t load_bytes;    /* bytes per weight load of a lane: 32, 16, 8, 4 or 2 */
+    int32_t rows_per_warp; /* 1, 2 or 4 */
+    int32_t pdl;           /* 1 = programmatic dependent launch */
+    int32_t ctas;          /* CTAs in the grid; 0 = no kernel (M == 0, or K == 0,
+                              where y is zero-filled by a memset) */
+    int32_t threads;       /* threads per CTA */
+    int32_t log2_segments; /* each row's K is cut into 2^log2_segments segments
+                              whose sums are combined in a fixed order */
+    int32_t x_in_smem;     /* 1 = x is staged in shared memory, 0 = read via L1 */
+} wsw_gemv_plan;
+
+/*
+ * wsw_gemv_bf16_plan -- the launch choices of wsw_gemv_bf16 (chain == 0) or of a link
+ * of wsw_gemv_bf16_chain (chain == 1) for these arguments, without launching anything
+ * or calling CUDA ([P4] "What shipped": the load width follows the alignment of the
+ * weight base and row pitch and degrades one step at a time; [P4] "Gates": a
+ * variant-selection test pins what the launcher picks).  The launchers take their
+ * choices from the same host function.
+ *
+ *   W          only its address is used (alignment); it is never dereferenced.
+ *   M, K, ld   as wsw_gemv_bf16, validated the same way.
+ *   sm_count   multiprocessors of the target device (> 0; 152 on GB300).
+ *   chain      0 or 1.
+ *   opts       as the call (NULL = defaults).
+ *   out        host struct, written on WSW_OK.
+ */
+int wsw_gemv_bf16_plan(const uint16_t *W, int64_t M, int64_t K, int64_t ld, int32_t sm_count,
+                       int32_t chain, const wsw_launch_opts *opts, wsw_gemv_plan *out);
+
 /*
  * wsw_gemv_q8_0 -- decode mat-vec with q8_0 weights and a q8_0 activation ([P3]
  * Scope: the quantized mat-vec behind the quantizer).
@@ -205,8 +238,10 @@ size_t wsw_moe_workspace_bytes(int64_t E, int64_t K, int64_t R);
  *   Wq   int8 [E][Mo][K];  Wd binary16 [E][Mo][K/32];  K % 32 == 0.
  *   xq   int8 [R][K];  xd binary16 [R][K/32].
  *   ids  int32 [R] (device).  A row whose id is outside [0, E) is skipped, its y
- *        row is left untouched, and *err_flag (if err_flag != NULL) is set to a
- *        nonzero value.  The library never clears *err_flag.
+ *        row is left untouched, and bit 0 of *err_flag (if err_flag != NULL) is
+ *        set.  Bit 1 is set if a bounded wait of the tensor-core form gave up (a
+ *        WSW_ERR_TIMEOUT condition); the y rows that CTA had not finished are then
+ *        NaN.  The library only ORs bits in; it never clears *err_flag.
  *   y    fp32 [R][Mo].
  *   ws   device workspace of ws_bytes >= wsw_moe_workspace_bytes(E, K, R) bytes,
  *        256-byte aligned, owned by the caller and overwritten by the call; NULL (or
@@ -276,6 +311,19 @@ int wsw_dequant_q8_0_kv(const int8_t *q, const uint16_t *d, int64_t depth, int64
  */
 int wsw_gemm_bf16(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const uint16_t *X,
                   int64_t N, int64_t ldx, float *Y, void *stream, const wsw_launch_opts *opts);
+
+/*
+ * wsw_bounded_wait_check -- run the bounded mbarrier wait of the tensor-core kernels
+ * on its own, one thread of one CTA.  The library has no device-side fault injection:
+ * this call is how the give-up path of a wait is exercised on a GPU.
+ *
+ *   arrive = 1   the barrier's phase completes before the wait: *status = WSW_OK.
+ *   arrive = 0   nothing completes the phase: the wait gives up after about one
+ *                second and *status = WSW_ERR_TIMEOUT.  The kernel then returns
+ *                normally and the context stays usable.
+ *   status       int32 on the device, written by the kernel.
+ */
+int wsw_bounded_wait_check(int32_t arrive, int32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert wsw.abi_version() == 2
+    assert wsw.abi_version() == 3
     assert wsw.status_string(0) == "WSW_OK"
     assert wsw.status_string(1) == "WSW_ERR_INVALID_ARG"
     assert wsw.status_string(2) == "WSW_ERR_MISALIGNED"
@@ -115,6 +115,10 @@ def test_other_calls_reject_on_host(lib):
     c = lib.wsw_gemv_bf16_chain
     assert c(-1, None, None, None) == INVALID
     assert c(0, None, None, None) == 0
+    b = lib.wsw_bounded_wait_check
+    assert b(2, P(4096), None) == INVALID
+    assert b(0, None, None) == INVALID
+    assert b(1, P(4098), None) == MISALIGNED
 
 
 def test_missing_library_raises(monkeypatch, tmp_path):

@@ -34,10 +34,10 @@ def _acts(orc, T, K, name):
     return orc.quantize_q8(x, 32)
 
 
-def _run(wsw, Wq, Wd, xq, xd, ids, opts=None):
+def _run(wsw, Wq, Wd, xq, xd, ids, opts=None, err_flag=None):
     return wsw.moe_gemv_q8_0(torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda(),
                              torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda(),
-                             torch.from_numpy(ids).cuda(), opts=opts)
+                             torch.from_numpy(ids).cuda(), opts=opts, err_flag=err_flag)
 
 
 @pytest.mark.parametrize("proj", ["gate_up", "down"])
@@ -48,7 +48,9 @@ def test_config_moe(orc, moe_weights, proj, T):
     Wq, Wd = moe_weights[proj]
     ids = syn.routing(0, "route%d" % T, T, E, TOPK).numpy()
     xq, xd = _acts(orc, T, K, proj)
-    y = _run(wsw, Wq, Wd, xq, xd, ids).cpu().numpy()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = _run(wsw, Wq, Wd, xq, xd, ids, err_flag=err).cpu().numpy()
+    assert err.item() == 0  # no bad id, and no bounded wait gave up
     R = T * TOPK
     rows = np.arange(R) if R <= 128 else np.unique(np.random.default_rng(T).integers(0, R, 64))
     for m in rows:
@@ -100,7 +102,7 @@ def test_bad_ids_set_the_flag_and_skip_rows(orc):
     wsw.moe_gemv_q8_0(torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda(),
                       torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda(),
                       torch.from_numpy(ids).cuda(), out=y, err_flag=err)
-    assert err.item() != 0
+    assert err.item() == 1  # bit 0: a bad id; no wait gave up
     yc = y.cpu().numpy()
     assert (yc[1] == 5.0).all() and (yc[3] == 5.0).all()
     y64, bad = orc.moe_gemv_q8_0(Wq, Wd, xq, xd, ids)
@@ -167,7 +169,7 @@ def test_tensor_core_form_against_oracle(orc, Mo, K, T, En, topk):
                           torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda(),
                           torch.from_numpy(ids).cuda(), out=y, err_flag=err, ws=ws)
         yc = y.cpu().numpy()
-        assert err.item() != 0
+        assert err.item() == 1  # bit 0: a bad id; no wait gave up
         assert np.isnan(yc[5]).all()
         for m in range(R):
             if m == 5:
@@ -202,7 +204,7 @@ def test_few_rows_gathered_form(orc, Mo, K, R):
         if ref is None:
             ref = y.clone()
         assert torch.equal(y.view(torch.int32), ref.view(torch.int32)), opts
-        assert (err.item() != 0) == bool((ids >= En).any())
+        assert err.item() == (1 if (ids >= En).any() else 0)
     for m in range(R):
         if ids[m] >= En:
             assert (ref[m] == 7.0).all()

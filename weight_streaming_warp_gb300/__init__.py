@@ -19,7 +19,8 @@ import torch
 __all__ = [
     "LaunchOpts", "WswError", "library_path", "load", "quantize_q8", "gemv_bf16",
     "gemv_bf16_chain", "gemv_q8_0", "quantize_gemv_q8_0", "moe_gemv_q8_0", "dequant_q8_0_kv", "gemm_bf16",
-    "upload_padded", "status_string", "abi_version", "moe_workspace_bytes",
+    "upload_padded", "status_string", "abi_version", "moe_workspace_bytes", "gemv_bf16_plan",
+    "bounded_wait_check",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,6 +43,11 @@ class _CLink(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("M", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("ld", ctypes.c_int64), ("x", ctypes.c_void_p), ("alpha", ctypes.c_float),
                 ("y", ctypes.c_void_p)]
+
+
+class _CPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("load_bytes", "rows_per_warp", "pdl", "ctas", "threads",
+                                               "log2_segments", "x_in_smem")]
 
 
 @dataclass
@@ -83,8 +89,11 @@ def load():
     L.wsw_moe_workspace_bytes.restype = ctypes.c_size_t
     L.wsw_dequant_q8_0_kv.argtypes = [_p, _p, _i64, _i64, _i64, _p, _p, _p]
     L.wsw_gemm_bf16.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _p, _p]
+    L.wsw_gemv_bf16_plan.argtypes = [_p, _i64, _i64, _i64, _i32, _i32, _p, _p]
+    L.wsw_bounded_wait_check.argtypes = [_i32, _p, _p]
     for f in ("wsw_quantize_q8", "wsw_gemv_bf16", "wsw_gemv_bf16_chain", "wsw_gemv_q8_0", "wsw_quantize_gemv_q8_0",
-              "wsw_moe_gemv_q8_0", "wsw_dequant_q8_0_kv", "wsw_gemm_bf16"):
+              "wsw_moe_gemv_q8_0", "wsw_dequant_q8_0_kv", "wsw_gemm_bf16", "wsw_gemv_bf16_plan",
+              "wsw_bounded_wait_check"):
         getattr(L, f).restype = ctypes.c_int
     _lib = L
     return L
@@ -271,6 +280,27 @@ def gemm_bf16(W, X, K=None, out=None, opts=None):
     _check(load().wsw_gemm_bf16(W.data_ptr(), M, K, ld, X.data_ptr(), N, ldx, Y.data_ptr(),
                                 _stream(), _opts(opts)), "gemm_bf16")
     return Y
+
+
+def gemv_bf16_plan(W_addr: int, M: int, K: int, ld: int, sm_count: int = 152, chain: bool = False,
+                   opts=None) -> dict:
+    """The launch that gemv_bf16 (chain=False) or a link of gemv_bf16_chain (chain=True)
+    makes for a weight matrix at device address W_addr (only its alignment matters),
+    as a dict of the wsw_gemv_plan fields.  Host only: no CUDA call."""
+    p = _CPlan()
+    _check(load().wsw_gemv_bf16_plan(ctypes.c_void_p(W_addr), M, K, ld, sm_count, int(bool(chain)),
+                                      _opts(opts), ctypes.byref(p)), "wsw_gemv_bf16_plan")
+    return {n: getattr(p, n) for n, _ in _CPlan._fields_}
+
+
+def bounded_wait_check(arrive: bool) -> torch.Tensor:
+    """Run the tensor-core kernels' bounded wait on its own; returns the int32 device
+    status it writes (0 = WSW_OK after an arrival, 6 = WSW_ERR_TIMEOUT after about a
+    second without one)."""
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _check(load().wsw_bounded_wait_check(int(bool(arrive)), status.data_ptr(), _stream()),
+           "wsw_bounded_wait_check")
+    return status
 
 
 def upload_padded(W: torch.Tensor, ld: int, device=None) -> torch.Tensor:

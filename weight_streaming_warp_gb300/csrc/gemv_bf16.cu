@@ -3,8 +3,8 @@
 // Source: "perf(vulkan): decode GEMV reads four elements per load, and the row lever
 // is dead" (vllm.cpp PR).  Opening paragraph: the decode GEMV moves ~52 GB of bf16
 // weights per token and is bound by DRAM bandwidth on weights streamed once.  "What
-// shipped": wider loads cut load instructions (here 16-byte loads, degrading to 8, 4
-// and 2 bytes when the base or row pitch is misaligned).  "What did NOT work": more
+// shipped": wider loads cut load instructions (here 32-byte loads, degrading to 16, 8,
+// 4 and 2 bytes when the base or row pitch is misaligned).  "What did NOT work": more
 // output rows per workgroup halves the number of independent sequential read streams;
 // results must be bit-identical for any rows-per-workgroup value.  Chaining: "cuda:
 // prefetch the next PTQ1_0 mat-vec's weights into L2 from the last CTAs", Overview and
@@ -156,6 +156,39 @@ int validate(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const float *x
 // (measured on GB300: 34816 x 5120 runs 2.6% faster than with two), two otherwise.  The
 // choice never changes a result bit.
 int auto_rows_per_warp(int64_t M) { return M >= 16384 ? 4 : 2; }
+bool rows_left_to_library(const wsw_launch_opts *opts) { return opts == nullptr || opts->rows_per_warp == 0; }
+
+// PDL: a single call follows opts->pdl (default off); a chain link is dependent unless
+// the caller passes options with pdl = 0.
+bool use_pdl(const wsw_launch_opts *opts, const Opts &o, bool chain) { return (chain && !opts) || o.pdl; }
+
+// Every choice of a launch, made on the host from the shape, the weight pointer's
+// alignment, the SM count and the options.  gemv_launch and wsw_gemv_bf16_plan both
+// take their choices from make_plan.
+struct Plan {
+    sg::Common c;
+    int rows_per_warp, load_bytes;
+    unsigned ctas;  // 0: no kernel
+    bool x_in_smem, pdl;
+    size_t x_smem;
+};
+
+int make_plan(const uint16_t *W, int64_t M, int64_t K, int64_t ld, int sm_count, const Opts &o, bool pdl,
+              bool auto_rows, Plan *p) {
+    *p = Plan{};
+    p->rows_per_warp = auto_rows ? auto_rows_per_warp(M) : o.rows_per_warp;
+    p->load_bytes = load_width(W, ld * 2, o.load_bytes);
+    p->pdl = pdl;
+    if (M == 0 || K == 0) return WSW_OK;
+    const int64_t nsteps = (K + Bf16::kStepElems - 1) / Bf16::kStepElems;
+    if (nsteps > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
+    p->c = sg::make_common(M, static_cast<int>(nsteps), p->rows_per_warp, sm_count, Bf16::kWarps, Bf16::kWarps);
+    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 16 / Bf16::kWarps;
+    p->ctas = sg::grid_ctas(p->c, static_cast<int64_t>(sm_count) * cps);
+    p->x_in_smem = nsteps <= kMaxSmemSteps;
+    p->x_smem = p->x_in_smem ? static_cast<size_t>(nsteps) * 2048 : 0;
+    return WSW_OK;
+}
 
 int gemv_launch(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const float *x, float alpha,
                 float *y, cudaStream_t s, const Opts &o, const DeviceInfo &di, bool pdl, bool auto_rows) {
@@ -163,18 +196,14 @@ int gemv_launch(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const float
     if (K == 0)
         return cudaMemsetAsync(y, 0, static_cast<size_t>(M) * 4, s) == cudaSuccess ? WSW_OK
                                                                                   : WSW_ERR_CUDA;
-    const int R = auto_rows ? auto_rows_per_warp(M) : o.rows_per_warp;
-    const int64_t nsteps = (K + Bf16::kStepElems - 1) / Bf16::kStepElems;
-    if (nsteps > 0x7fffffffLL) return WSW_ERR_UNSUPPORTED;
+    Plan p;
+    const int st = make_plan(W, M, K, ld, di.sm_count, o, pdl, auto_rows, &p);
+    if (st != WSW_OK) return st;
     Bf16::Args a;
-    a.c = sg::make_common(M, static_cast<int>(nsteps), R, di.sm_count, Bf16::kWarps, Bf16::kWarps);
+    a.c = p.c;
     a.W = W; a.K = K; a.ld = ld; a.x = x; a.alpha = alpha; a.y = y;
-    const int cps = o.ctas_per_sm > 0 ? o.ctas_per_sm : 16 / Bf16::kWarps;
-    const unsigned ctas = sg::grid_ctas(a.c, static_cast<int64_t>(di.sm_count) * cps);
-    const bool xs = nsteps <= kMaxSmemSteps;
-    const size_t x_smem = xs ? static_cast<size_t>(nsteps) * 2048 : 0;
-    const int lb = load_width(W, ld * 2, o.load_bytes);
-    const cudaError_t e = sg::launch_stream_gemv<Bf16>(R, lb, xs, a, ctas, x_smem, s, pdl);
+    const cudaError_t e =
+        sg::launch_stream_gemv<Bf16>(p.rows_per_warp, p.load_bytes, p.x_in_smem, a, p.ctas, p.x_smem, s, p.pdl);
     return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
 }
 
@@ -191,8 +220,8 @@ extern "C" int wsw_gemv_bf16(const uint16_t *W, int64_t M, int64_t K, int64_t ld
     if (st != WSW_OK || M == 0) return st;
     DeviceInfo di;
     if (!device_info(&di, &st)) return st;
-    return gemv_launch(W, M, K, ld, x, alpha, y, static_cast<cudaStream_t>(stream), o, di, o.pdl,
-                       opts == nullptr || opts->rows_per_warp == 0);
+    return gemv_launch(W, M, K, ld, x, alpha, y, static_cast<cudaStream_t>(stream), o, di,
+                       use_pdl(opts, o, false), rows_left_to_library(opts));
 }
 
 extern "C" int wsw_gemv_bf16_chain(int64_t n_links, const wsw_gemv_link *links, void *stream,
@@ -210,14 +239,36 @@ extern "C" int wsw_gemv_bf16_chain(int64_t n_links, const wsw_gemv_link *links, 
     if (n_links == 0) return WSW_OK;
     DeviceInfo di;
     if (!device_info(&di, &st)) return st;
-    // Default for a chain is PDL on; an explicit opts->pdl = 0 turns it off.
-    const bool pdl = opts ? o.pdl : true;
+    const bool pdl = use_pdl(opts, o, true);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (int64_t i = 0; i < n_links; ++i) {
         const wsw_gemv_link &l = links[i];
-        st = gemv_launch(l.W, l.M, l.K, l.ld, l.x, l.alpha, l.y, s, o, di, pdl,
-                         opts == nullptr || opts->rows_per_warp == 0);
+        st = gemv_launch(l.W, l.M, l.K, l.ld, l.x, l.alpha, l.y, s, o, di, pdl, rows_left_to_library(opts));
         if (st != WSW_OK) return st;
     }
+    return WSW_OK;
+}
+
+extern "C" int wsw_gemv_bf16_plan(const uint16_t *W, int64_t M, int64_t K, int64_t ld, int32_t sm_count,
+                                  int32_t chain, const wsw_launch_opts *opts, wsw_gemv_plan *out) {
+    using namespace wsw;
+    if (!out || sm_count <= 0 || (chain != 0 && chain != 1)) return WSW_ERR_INVALID_ARG;
+    Opts o;
+    int st = resolve_opts(opts, &o);
+    if (st != WSW_OK) return st;
+    // x and y are not part of the plan: stand-ins that pass their checks
+    static const float stand_in[1] = {0.f};
+    st = validate(W, M, K, ld, stand_in, stand_in);
+    if (st != WSW_OK) return st;
+    Plan p;
+    st = make_plan(W, M, K, ld, sm_count, o, use_pdl(opts, o, chain == 1), rows_left_to_library(opts), &p);
+    if (st != WSW_OK) return st;
+    out->load_bytes = p.load_bytes;
+    out->rows_per_warp = p.rows_per_warp;
+    out->pdl = p.pdl ? 1 : 0;
+    out->ctas = static_cast<int32_t>(p.ctas);
+    out->threads = p.ctas ? Bf16::kWarps * 32 : 0;
+    out->log2_segments = p.ctas ? p.c.log2_seg : 0;
+    out->x_in_smem = p.x_in_smem ? 1 : 0;
     return WSW_OK;
 }

@@ -43,6 +43,10 @@
 //                  takes the blocks of parity h and hands its sums to group 0 through
 //                  shared memory, with more it takes every block for columns 32 h ..
 //                  32 h + 31
+//  * Every mbarrier wait gives up after about a second (tc_util.cuh).  A warp whose wait
+//    ran out stops its role, the epilogue writes NaN into the rows of the CTA's
+//    remaining items, and the kernel sets bit 1 (value 2) of the caller's error flag.
+//    Bad expert ids set bit 0.
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -121,6 +125,8 @@ struct Smem {
     uint64_t s_full[2], s_empty[2];
     uint32_t tmem_slot;
     int nitems;
+    int timed_out;  // an epilogue wait ran out (a wait that runs out anywhere stops the
+                    // data reaching the epilogue, so the epilogue's waits run out too)
 };
 
 // byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled K-major tile
@@ -445,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         S.ibase[E] = hdr[1 + 3 * E];
         S.nitems = hdr[0];
+        S.timed_out = 0;
     }
     __syncthreads();
     pdl_launch_dependents();
@@ -697,9 +704,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("bar.sync 1, 256;" ::: "memory");
             }
         }
+        if (!ok) S.timed_out = 1;  // the rows of the remaining items hold NaN
     }
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0 && S.timed_out && a.err) atomicOr(a.err, 2);  // tell the host
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");

@@ -11,6 +11,9 @@ namespace wsw {
 namespace tc {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+// A second bound that does not depend on the timer: even at one poll per cycle this
+// many polls take longer than kWaitLimitNs, so it only ends a wait whose clock stalls.
+constexpr uint32_t kWaitMaxPolls = 1u << 31;
 
 __device__ __forceinline__ uint32_t saddr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -28,8 +31,9 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Wait for the phase with the given parity to complete; give up after kWaitLimitNs.
-// The clock is read only once a wait has already spun for a while.
+// Wait for the phase with the given parity to complete; give up (return false) after
+// kWaitLimitNs or kWaitMaxPolls polls.  The clock and the poll count are checked only
+// once a wait has already spun for a while.
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
     uint64_t t0 = 0;
     for (uint32_t i = 1;; ++i) {
@@ -41,6 +45,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
             : "memory");
         if (done) return true;
         if ((i & 1023u) == 0) {
+            if (i >= kWaitMaxPolls) return false;
             const uint64_t t = global_ns();
             if (t0 == 0) t0 = t;
             else if (t - t0 > kWaitLimitNs) return false;
