@@ -351,19 +351,21 @@ def measure_chain(torch, wsw, dev):
     nbytes = sum(Mi * Ki * 2 + Ki * 4 + Mi * 4 for (Mi, Ki) in shapes)
     res = {}
     graphs = {}
-    for pdl in (1, 0):
-        graphs[pdl] = _graph(torch, lambda stream, pdl=pdl: wsw.gemv_bf16_chain(links, opts={"pdl": pdl}))
-        _time_graph(torch, graphs[pdl], 2)
-    t = {1: [], 0: []}
+    # the library's chain (PDL), plain stream order, and PDL plus an L2 prefetch of each
+    # next link's first loads by the finishing warps (off by default: it measured slower)
+    arms = {"pdl": {"pdl": 1}, "no_pdl": {"pdl": 0}, "pdl_l2_prefetch_4": {"pdl": 1, "l2_prefetch_steps": 4}}
+    for name, o in arms.items():
+        graphs[name] = _graph(torch, lambda stream, o=o: wsw.gemv_bf16_chain(links, opts=o))
+        _time_graph(torch, graphs[name], 2)
+    t = {name: [] for name in arms}
     for rep in range(6):  # paired, alternating order
-        for pdl in ((1, 0) if rep % 2 == 0 else (0, 1)):
-            t[pdl].append(_time_graph(torch, graphs[pdl], 1))
-    for pdl in (1, 0):
-        med = statistics.median(t[pdl])
-        res["pdl" if pdl else "no_pdl"] = {"ms_per_token": round(med * 1e3, 4),
-                                          "GBps": round(nbytes / med / 1e9, 1),
-                                          "tok_per_s": round(1.0 / med, 2),
-                                          "min_ms": round(min(t[pdl]) * 1e3, 4), "max_ms": round(max(t[pdl]) * 1e3, 4)}
+        for name in (list(arms) if rep % 2 == 0 else list(arms)[::-1]):
+            t[name].append(_time_graph(torch, graphs[name], 1))
+    for name in arms:
+        med = statistics.median(t[name])
+        res[name] = {"ms_per_token": round(med * 1e3, 4), "GBps": round(nbytes / med / 1e9, 1),
+                     "tok_per_s": round(1.0 / med, 2),
+                     "min_ms": round(min(t[name]) * 1e3, 4), "max_ms": round(max(t[name]) * 1e3, 4)}
     ok = all(bool(torch.isfinite(y).all()) for y in ys[-2:])
     del graphs, Ws, ys, links
     torch.cuda.empty_cache()

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define WSW_ABI_VERSION 3
+#define WSW_ABI_VERSION 4
 
 typedef enum wsw_status {
     WSW_OK = 0,
@@ -63,6 +63,12 @@ typedef enum wsw_status {
                                 device: wsw_bounded_wait_check, bit 1 of the MoE
                                 error flag) */
 } wsw_status;
+
+/* Steps of the next link that a chain link prefetches into L2 by default: 0 = off.
+ * Programmatic dependent launch already issues each link's first loads while the one
+ * before drains; on GB300 the 257-link 27B-shaped chain ran 0.4% (2 steps) to 3.8%
+ * (16 steps) slower with the prefetch on. */
+#define WSW_CHAIN_L2_PREFETCH_STEPS 0
 
 /* Launch knobs.  Pass NULL for the defaults.  0 in a field means "choose". */
 typedef struct wsw_launch_opts {
@@ -77,6 +83,11 @@ typedef struct wsw_launch_opts {
                               for the previous kernel in the stream ([P5]
                               "Additional information": PDL on sm_90 and newer) */
     int32_t ctas_per_sm;   /* resident CTAs per SM for persistent grids; 0 = auto */
+    int32_t l2_prefetch_steps; /* wsw_gemv_bf16_chain only: once done with a link,
+                              its warps request into L2 the first this-many 1 KB steps
+                              of every warp's first unit of the next link ([P5]
+                              Overview); 1..64, -1 = off, 0 = the library's choice
+                              (WSW_CHAIN_L2_PREFETCH_STEPS) */
 } wsw_launch_opts;
 
 /* Human-readable name of a wsw_status value (static storage, never NULL). */
@@ -157,6 +168,8 @@ typedef struct wsw_gemv_plan {
     int32_t log2_segments; /* each row's K is cut into 2^log2_segments segments
                               whose sums are combined in a fixed order */
     int32_t x_in_smem;     /* 1 = x is staged in shared memory, 0 = read via L1 */
+    int32_t l2_prefetch_steps; /* chain links: steps of the next link's first units
+                              requested into L2 (0 = none; the last link has no next) */
 } wsw_gemv_plan;
 
 /*

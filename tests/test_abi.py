@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert wsw.abi_version() == 3
+    assert wsw.abi_version() == 4
     assert wsw.status_string(0) == "WSW_OK"
     assert wsw.status_string(1) == "WSW_ERR_INVALID_ARG"
     assert wsw.status_string(2) == "WSW_ERR_MISALIGNED"
@@ -50,7 +50,8 @@ P = ctypes.c_void_p
 
 class _Opts(ctypes.Structure):
     _fields_ = [("rows_per_warp", ctypes.c_int32), ("load_bytes", ctypes.c_int32),
-                ("pdl", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32)]
+                ("pdl", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
+                ("l2_prefetch_steps", ctypes.c_int32)]
 
 
 def test_quantize_rejects_on_host(lib):

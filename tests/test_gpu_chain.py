@@ -95,3 +95,24 @@ def test_many_links_in_a_cuda_graph(orc):
     wsw.gemv_bf16_chain(links, opts={"pdl": 0})
     for a, b in zip(graph_out, ys):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("steps", [-1, 1, 4, 64])
+def test_l2_prefetch_of_the_next_link_changes_no_bit(orc, steps):
+    """The finishing warps of each link request the next link's first loads into L2
+    (a padded, ragged last link included); the outputs stay bit for bit those of the
+    links launched one at a time."""
+    wsw = need_gpu()
+    shapes = _links(1) + [("ragged", 1000, 4104)]
+    Ws, ys, x0, links = _build(shapes, seed=2)
+    Wp = wsw.upload_padded(Ws[-1], 4104 + 64)  # the last link reads a padded matrix
+    links[-1] = (Wp, 4104) + links[-1][2:]
+    wsw.gemv_bf16_chain(links, opts={"pdl": 1, "l2_prefetch_steps": steps})
+    torch.cuda.synchronize()
+    chained = [y.clone() for y in ys]
+    for (W, K, x, a, y) in links:
+        wsw.gemv_bf16(W, x, alpha=a, K=K, out=y)
+    for a, b in zip(chained, ys):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    ref = _oracle_chain(orc, Ws, x0, shapes)
+    _assert_chain_close(ys, ref, "prefetching chain")

@@ -44,6 +44,24 @@ def test_load_bytes_option_caps_and_never_widens():
     assert plan(addr=BASE + 2, opts=LaunchOpts(load_bytes=32))["load_bytes"] == 2
 
 
+def _header_default_prefetch():
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = open(os.path.join(root, "include", "wsw.h")).read()
+    return int(re.search(r"#define WSW_CHAIN_L2_PREFETCH_STEPS (\d+)", src).group(1))
+
+
+def test_chain_l2_prefetch_of_the_next_link():
+    assert plan()["l2_prefetch_steps"] == 0                          # a single call has no next link
+    assert plan(chain=True)["l2_prefetch_steps"] == _header_default_prefetch()
+    assert plan(chain=True, opts=LaunchOpts(l2_prefetch_steps=4))["l2_prefetch_steps"] == 4
+    assert plan(chain=True, opts=LaunchOpts(l2_prefetch_steps=-1))["l2_prefetch_steps"] == 0
+    for bad in (-2, 65):
+        with pytest.raises(WswError, match="INVALID_ARG"):
+            plan(chain=True, opts=LaunchOpts(l2_prefetch_steps=bad))
+
+
 def test_pdl_defaults():
     assert plan()["pdl"] == 0                                       # single call: off
     assert plan(opts=LaunchOpts(pdl=1))["pdl"] == 1

@@ -36,7 +36,8 @@ class WswError(RuntimeError):
 
 class _COpts(ctypes.Structure):
     _fields_ = [("rows_per_warp", ctypes.c_int32), ("load_bytes", ctypes.c_int32),
-                ("pdl", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32)]
+                ("pdl", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
+                ("l2_prefetch_steps", ctypes.c_int32)]
 
 
 class _CLink(ctypes.Structure):
@@ -47,7 +48,7 @@ class _CLink(ctypes.Structure):
 
 class _CPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("load_bytes", "rows_per_warp", "pdl", "ctas", "threads",
-                                               "log2_segments", "x_in_smem")]
+                                               "log2_segments", "x_in_smem", "l2_prefetch_steps")]
 
 
 @dataclass
@@ -57,9 +58,10 @@ class LaunchOpts:
     load_bytes: int = 0
     pdl: int = 0
     ctas_per_sm: int = 0
+    l2_prefetch_steps: int = 0  # chain only: -1 = off
 
     def _c(self):
-        return _COpts(self.rows_per_warp, self.load_bytes, self.pdl, self.ctas_per_sm)
+        return _COpts(self.rows_per_warp, self.load_bytes, self.pdl, self.ctas_per_sm, self.l2_prefetch_steps)
 
 
 def library_path() -> str:

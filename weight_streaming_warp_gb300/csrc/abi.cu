@@ -51,7 +51,7 @@ bool device_info(DeviceInfo *out, int *status) {
 }
 
 int resolve_opts(const wsw_launch_opts *o, Opts *out) {
-    Opts r{2, 32, false, 0};
+    Opts r{2, 32, false, 0, WSW_CHAIN_L2_PREFETCH_STEPS};
     if (o) {
         if (o->rows_per_warp != 0) {
             if (o->rows_per_warp != 1 && o->rows_per_warp != 2 && o->rows_per_warp != 4)
@@ -68,6 +68,8 @@ int resolve_opts(const wsw_launch_opts *o, Opts *out) {
         r.pdl = o->pdl == 1;
         if (o->ctas_per_sm < 0 || o->ctas_per_sm > 32) return WSW_ERR_INVALID_ARG;
         r.ctas_per_sm = o->ctas_per_sm;
+        if (o->l2_prefetch_steps < -1 || o->l2_prefetch_steps > 64) return WSW_ERR_INVALID_ARG;
+        if (o->l2_prefetch_steps != 0) r.l2_prefetch_steps = o->l2_prefetch_steps < 0 ? 0 : o->l2_prefetch_steps;
     }
     *out = r;
     return WSW_OK;

@@ -159,6 +159,7 @@ struct Opts {
     int load_bytes;
     bool pdl;
     int ctas_per_sm;
+    int l2_prefetch_steps;  // resolved: 0 = off
 };
 int resolve_opts(const wsw_launch_opts *o, Opts *out);
 

@@ -40,6 +40,7 @@ struct Bf16 {
         const float *x;
         float alpha;
         float *y;
+        sg::NextLink nx;  // the next link of a chain (nx.W == NULL: none)
     };
     __device__ __forceinline__ static const char *row_ptr(const Args &a, int64_t row) {
         return reinterpret_cast<const char *>(a.W + row * a.ld);
@@ -190,8 +191,27 @@ int make_plan(const uint16_t *W, int64_t M, int64_t K, int64_t ld, int sm_count,
     return WSW_OK;
 }
 
+// What a chain link needs to know of the next link to prefetch its first loads: the
+// next link's own plan, under the same options.
+sg::NextLink next_link(const wsw_gemv_link &l, int sm_count, const Opts &o, bool pdl, bool auto_rows) {
+    sg::NextLink nx{};
+    Plan p;
+    if (o.l2_prefetch_steps <= 0 ||
+        make_plan(l.W, l.M, l.K, l.ld, sm_count, o, pdl, auto_rows, &p) != WSW_OK || p.ctas == 0)
+        return nx;
+    nx.W = reinterpret_cast<const char *>(l.W);
+    nx.pitch = l.ld * 2;
+    nx.row_bytes = l.K * 2;
+    nx.c = p.c;
+    nx.ctas = static_cast<int>(p.ctas);
+    nx.R = p.rows_per_warp;
+    nx.steps = o.l2_prefetch_steps;
+    return nx;
+}
+
 int gemv_launch(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const float *x, float alpha,
-                float *y, cudaStream_t s, const Opts &o, const DeviceInfo &di, bool pdl, bool auto_rows) {
+                float *y, cudaStream_t s, const Opts &o, const DeviceInfo &di, bool pdl, bool auto_rows,
+                const sg::NextLink &nx) {
     if (M == 0) return WSW_OK;
     if (K == 0)
         return cudaMemsetAsync(y, 0, static_cast<size_t>(M) * 4, s) == cudaSuccess ? WSW_OK
@@ -202,6 +222,7 @@ int gemv_launch(const uint16_t *W, int64_t M, int64_t K, int64_t ld, const float
     Bf16::Args a;
     a.c = p.c;
     a.W = W; a.K = K; a.ld = ld; a.x = x; a.alpha = alpha; a.y = y;
+    a.nx = nx;
     const cudaError_t e =
         sg::launch_stream_gemv<Bf16>(p.rows_per_warp, p.load_bytes, p.x_in_smem, a, p.ctas, p.x_smem, s, p.pdl);
     return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
@@ -221,7 +242,7 @@ extern "C" int wsw_gemv_bf16(const uint16_t *W, int64_t M, int64_t K, int64_t ld
     DeviceInfo di;
     if (!device_info(&di, &st)) return st;
     return gemv_launch(W, M, K, ld, x, alpha, y, static_cast<cudaStream_t>(stream), o, di,
-                       use_pdl(opts, o, false), rows_left_to_library(opts));
+                       use_pdl(opts, o, false), rows_left_to_library(opts), sg::NextLink{});
 }
 
 extern "C" int wsw_gemv_bf16_chain(int64_t n_links, const wsw_gemv_link *links, void *stream,
@@ -239,11 +260,13 @@ extern "C" int wsw_gemv_bf16_chain(int64_t n_links, const wsw_gemv_link *links, 
     if (n_links == 0) return WSW_OK;
     DeviceInfo di;
     if (!device_info(&di, &st)) return st;
-    const bool pdl = use_pdl(opts, o, true);
+    const bool pdl = use_pdl(opts, o, true), auto_rows = rows_left_to_library(opts);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (int64_t i = 0; i < n_links; ++i) {
         const wsw_gemv_link &l = links[i];
-        st = gemv_launch(l.W, l.M, l.K, l.ld, l.x, l.alpha, l.y, s, o, di, pdl, rows_left_to_library(opts));
+        const sg::NextLink nx =
+            i + 1 < n_links ? next_link(links[i + 1], di.sm_count, o, pdl, auto_rows) : sg::NextLink{};
+        st = gemv_launch(l.W, l.M, l.K, l.ld, l.x, l.alpha, l.y, s, o, di, pdl, auto_rows, nx);
         if (st != WSW_OK) return st;
     }
     return WSW_OK;
@@ -270,5 +293,6 @@ extern "C" int wsw_gemv_bf16_plan(const uint16_t *W, int64_t M, int64_t K, int64
     out->threads = p.ctas ? Bf16::kWarps * 32 : 0;
     out->log2_segments = p.ctas ? p.c.log2_seg : 0;
     out->x_in_smem = p.x_in_smem ? 1 : 0;
+    out->l2_prefetch_steps = chain ? o.l2_prefetch_steps : 0;
     return WSW_OK;
 }

@@ -31,9 +31,13 @@
 // lane_total / store.  load_x also receives the first row of the group (a format whose
 // activation differs by row picks it from there).  kWaitFirst: the weight addresses
 // depend on data written by earlier kernels, so the dependency wait and stage_x come
-// before the first weight load.
+// before the first weight load.  A format whose Args has a NextLink `nx` also requests
+// into L2, once its warps are done, what the next mat-vec of a chain reads first.
 // A step is 1 KB of a row in both formats.
 #pragma once
+
+#include <type_traits>
+#include <utility>
 
 #include "common.cuh"
 
@@ -62,6 +66,52 @@ struct Common {
 // First step of K-segment k of an n-step row cut into 2^ls segments.
 __host__ __device__ __forceinline__ int seg_begin(int k, int n, int ls) {
     return static_cast<int>((static_cast<int64_t>(k) * n) >> ls);
+}
+
+// The next mat-vec of a chain, as far as its first loads go.
+struct NextLink {
+    const char *W;      // its weights; NULL: no next link, or nothing to prefetch
+    int64_t pitch;      // row stride in bytes
+    int64_t row_bytes;  // bytes of a row that are read
+    Common c;           // its decomposition
+    int ctas;           // its grid
+    int R;              // its rows per warp
+    int steps;          // steps of each warp's first unit to request
+};
+
+template <class F, class = void>
+struct HasNextLink : std::false_type {};
+template <class F>
+struct HasNextLink<F, std::void_t<decltype(std::declval<typename F::Args>().nx)>> : std::true_type {};
+
+// L2 prefetch of the next link's first loads ("cuda: prefetch the next PTQ1_0 mat-vec's
+// weights into L2 from the last CTAs", Overview: CTAs that are done with the current
+// mat-vec request the next one's weights while the rest drain).  The next launch's CTA
+// n starts with block n, whose unit for warp w is (n << lb) + w; that warp first loads
+// the first steps of the unit's rows.  Warp w of this launch's CTA c requests the first
+// nx.steps steps of warp w's first unit for the next CTAs c, c + C, ... (both launches
+// have NW warps per CTA).  Off unless the chain asks for it: on GB300 the chain ran
+// slower with it, PDL's pre-wait loads already covering the transition.
+template <int NW>
+__device__ __forceinline__ void prefetch_next_link(const NextLink &nx, int wid, int lane) {
+    if (nx.W == nullptr || nx.steps <= 0) return;
+    constexpr int kLines = kStepBytes / 128;
+    const int ls = nx.c.log2_seg, lb = nx.c.log2_block;
+    for (int64_t n = blockIdx.x; n < nx.ctas; n += gridDim.x) {
+        const int64_t u = (n << lb) + wid;
+        const int64_t g = u >> ls;
+        if (g >= nx.c.groups) continue;
+        const int k = static_cast<int>(u & ((1 << ls) - 1));
+        const int st = seg_begin(k, nx.c.nsteps, ls);
+        const int se = seg_begin(k + 1, nx.c.nsteps, ls);
+        const int ns = nx.steps < se - st ? nx.steps : se - st;
+        for (int i = lane; i < nx.R * ns * kLines; i += 32) {
+            const int line = i % kLines, rs = i / kLines;
+            const int64_t row = g * nx.R + rs % nx.R;
+            const int64_t off = static_cast<int64_t>(st + rs / nx.R) * kStepBytes + line * 128;
+            if (row < nx.c.M && off < nx.row_bytes) prefetch_l2(nx.W + row * nx.pitch + off);
+        }
+    }
 }
 
 template <class F, int R, int LB, bool XS, bool SPLIT>
@@ -259,6 +309,7 @@ __global__ void __launch_bounds__(F::kWarps * 32, 16 / F::kWarps) stream_gemv_ke
         pdl_wait();
         pdl_launch_dependents();
     }
+    if constexpr (HasNextLink<F>::value) prefetch_next_link<NW>(a.nx, wid, lane);
 }
 
 // K-segments per row (log2) for an M x (nsteps warp steps) matrix on `sm_count` SMs and
