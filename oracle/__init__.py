@@ -38,6 +38,8 @@ def lib():
         L.orc_gemm_bf16.restype = None
         L.orc_dequant_q8_0_kv.argtypes = [p, p, i64, i64, i64, p]
         L.orc_dequant_q8_0_kv.restype = None
+        L.orc_attn_decode.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, i64, i64, ctypes.c_double, p]
+        L.orc_attn_decode.restype = None
         _lib = L
     return _lib
 
@@ -146,4 +148,26 @@ def dequant_q8_0_kv(q, d_bits):
     depth, heads, hd = q.shape
     out = np.zeros((heads, depth, hd), np.uint16)
     lib().orc_dequant_q8_0_kv(_ptr(q), _ptr(d), depth, heads, hd, _ptr(out))
+    return out
+
+
+def attn_decode(q, k_bits, v_bits, scale, layout="per_head"):
+    """q fp32 [heads][group][head_dim]; k, v uint16 (binary16 bits) laid out
+    [heads][depth][head_dim] (layout "per_head") or [depth][heads][head_dim]
+    ("position_major") -> out fp64 [heads][group][head_dim]."""
+    q = _c(q, np.float32)
+    k = _c(k_bits, np.uint16)
+    v = _c(v_bits, np.uint16)
+    heads, group, hd = q.shape
+    if layout == "per_head":
+        depth = k.shape[1]
+        ps, hs = hd, depth * hd
+    elif layout == "position_major":
+        depth = k.shape[0]
+        ps, hs = heads * hd, hd
+    else:
+        raise ValueError(layout)
+    out = np.zeros((heads, group, hd), np.float64)
+    lib().orc_attn_decode(_ptr(q), _ptr(k), _ptr(v), depth, heads, group, hd, ps, hs, ps, hs,
+                          float(scale), _ptr(out))
     return out

@@ -41,6 +41,7 @@
  * Build: gcc -O2 -std=c99 -ffp-contract=off -fPIC -shared (see oracle/build.py).
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -288,4 +289,54 @@ void orc_dequant_q8_0_kv(const int8_t *q, const uint16_t *d, int64_t depth, int6
             }
         }
     }
+}
+
+/* ---------------------------------------------------------------------------
+ * attn_decode  ([P1] Overview: the flash-attention pass reads the dequantized
+ * binary16 K and V of every cached position; the stride discussion gives the two
+ * layouts it can read them in)
+ *
+ * One decoding step of scaled dot-product attention over `depth` cached positions,
+ * for `heads` KV heads with `group` query heads each (grouped-query attention):
+ *   s_p          = scale * sum_i q[h][g][i] * K(h, p)[i]
+ *   out[h][g][i] = sum_p exp(s_p - m) * V(h, p)[i] / sum_p exp(s_p - m),
+ *                  m = max_p s_p
+ * (subtracting m changes nothing mathematically; it keeps exp finite).  K(h, p) is
+ * the binary16 row that starts k_head_stride * h + k_pos_stride * p elements into k:
+ * the per-head-contiguous scratch has (k_pos_stride, k_head_stride) =
+ * (head_dim, depth * head_dim), the position-major cache (head_dim * heads,
+ * head_dim).  V likewise.  q is fp32 [heads][group][head_dim]; out is fp64
+ * [heads][group][head_dim].  All arithmetic in fp64, exp from libm.
+ * ------------------------------------------------------------------------- */
+void orc_attn_decode(const float *q, const uint16_t *k, const uint16_t *v, int64_t depth,
+                     int64_t heads, int64_t group, int64_t head_dim, int64_t k_pos_stride,
+                     int64_t k_head_stride, int64_t v_pos_stride, int64_t v_head_stride,
+                     double scale, double *out)
+{
+    double *s = (double *)malloc((size_t)(depth > 0 ? depth : 1) * sizeof(double));
+    for (int64_t h = 0; h < heads; ++h) {
+        for (int64_t g = 0; g < group; ++g) {
+            const float *qv = q + (h * group + g) * head_dim;
+            double *o = out + (h * group + g) * head_dim;
+            double m = -HUGE_VAL;
+            for (int64_t p = 0; p < depth; ++p) {
+                const uint16_t *kr = k + h * k_head_stride + p * k_pos_stride;
+                double dot = 0.0;
+                for (int64_t i = 0; i < head_dim; ++i)
+                    dot += (double)qv[i] * (double)orc_f16_to_f32(kr[i]);
+                s[p] = scale * dot;
+                if (s[p] > m) m = s[p];
+            }
+            double den = 0.0;
+            for (int64_t i = 0; i < head_dim; ++i) o[i] = 0.0;
+            for (int64_t p = 0; p < depth; ++p) {
+                const uint16_t *vr = v + h * v_head_stride + p * v_pos_stride;
+                double w = exp(s[p] - m);
+                den += w;
+                for (int64_t i = 0; i < head_dim; ++i) o[i] += w * (double)orc_f16_to_f32(vr[i]);
+            }
+            for (int64_t i = 0; i < head_dim; ++i) o[i] /= den;
+        }
+    }
+    free(s);
 }
