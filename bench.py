@@ -440,6 +440,38 @@ def measure_rows(torch, wsw, dev):
         out["dequant_kv_d%d" % depth] = {"us": round(t * 1e6, 2), "GBps": round(nb / t / 1e9, 1),
                                          "us_pdl": round(tp * 1e6, 2), "GBps_pdl": round(nb / tp / 1e9, 1)}
         del qs, ds
+    # decode attention over the binary16 KV (4 KV heads x 128; groups of 1 and 8 query
+    # heads), reading the per-head scratch and the position-major cache; 4 copies of K
+    # and V rotate (268 MB and more)
+    for depth in (32768, 65536):
+        copies = 4
+        Ks = [torch.randn((4, depth, 128), generator=g, device=dev).half() for _ in range(copies)]
+        Vs = [torch.randn((4, depth, 128), generator=g, device=dev).half() for _ in range(copies)]
+        Kc = [t.permute(1, 0, 2).contiguous() for t in Ks]
+        Vc = [t.permute(1, 0, 2).contiguous() for t in Vs]
+        for group in (1, 8):
+            qq = torch.randn((4, group, 128), generator=g, device=dev)
+            o = torch.empty((4, group, 128), dtype=torch.float32, device=dev)
+            ws = torch.empty(wsw.attn_decode_workspace_bytes(depth, 4, group), dtype=torch.uint8, device=dev)
+            for layout in ("per_head", "position_major"):
+                it = [0]
+
+                def make(pdl, qq=qq, o=o, ws=ws, layout=layout, it=it):
+                    def fn(stream):
+                        i = it[0] % copies
+                        it[0] += 1
+                        if layout == "per_head":
+                            k, v = Ks[i], Vs[i]
+                        else:
+                            k, v = Kc[i].permute(1, 0, 2), Vc[i].permute(1, 0, 2)
+                        wsw.attn_decode_f16(qq, k, v, out=o, ws=ws, opts={"pdl": pdl})
+                    return fn
+                t, tp = _rate_both(torch, make, 32)
+                nb = 2 * depth * 4 * 128 * 2 + 2 * 4 * group * 128 * 4
+                out["attn_decode_d%d_g%d_%s" % (depth, group, layout)] = {
+                    "us": round(t * 1e6, 2), "GBps": round(nb / t / 1e9, 1),
+                    "us_pdl": round(tp * 1e6, 2), "GBps_pdl": round(nb / tp / 1e9, 1)}
+        del Ks, Vs, Kc, Vc
     # grouped MoE mat-vec (gate_up: 1536 x 2048 per expert), 128 experts, top-8; calls
     # rotate over 8 routings and 2 copies of the expert weights (2 x 403 MB), so the
     # experts a call reads are not left in L2 by the call before

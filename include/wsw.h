@@ -51,13 +51,14 @@
 extern "C" {
 #endif
 
-#define WSW_ABI_VERSION 4
+#define WSW_ABI_VERSION 5
 
 typedef enum wsw_status {
     WSW_OK = 0,
     WSW_ERR_INVALID_ARG = 1, /* null pointer, bad size, stride or block size */
     WSW_ERR_MISALIGNED = 2,  /* alignment that the call cannot degrade around */
     WSW_ERR_UNSUPPORTED = 3, /* device is not sm_103 / shape beyond a stated limit */
+    WSW_ERR_WORKSPACE = 4,   /* a required caller workspace is absent or too small */
     WSW_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
     WSW_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up (read on the
                                 device: wsw_bounded_wait_check, bit 1 of the MoE
@@ -308,6 +309,38 @@ int wsw_moe_gemv_q8_0_noalloc(const int8_t *Wq, const uint16_t *Wd, int64_t E, i
  */
 int wsw_dequant_q8_0_kv(const int8_t *q, const uint16_t *d, int64_t depth, int64_t heads,
                         int64_t head_dim, uint16_t *out, void *stream,
+                        const wsw_launch_opts *opts);
+
+/*
+ * wsw_attn_decode_f16 -- one decoding step of attention over a binary16 KV cache, the
+ * consumer of the dequantized scratch ([P1] Overview: the flash-attention pass reads
+ * the f16 K and V; the stride discussion: the cache keeps one head's rows
+ * head_dim * n_head_kv elements apart, the scratch back to back).
+ *
+ *   s_p          = scale * sum_i q[h][g][i] * K(h, p)[i]
+ *   out[h][g][i] = sum_p exp(s_p - m) * V(h, p)[i] / sum_p exp(s_p - m),  m = max_p s_p
+ * over every position p < depth, for `heads` KV heads with `group` query heads each.
+ * K(h, p) is the row of head_dim binary16 values at k + h * k_head_stride +
+ * p * k_pos_stride (elements); V likewise.  The per-head-contiguous scratch that
+ * wsw_dequant_q8_0_kv writes has (pos, head) strides (head_dim, depth * head_dim), the
+ * position-major cache (heads * head_dim, head_dim).  fp32 arithmetic; results agree
+ * with fp64 within 1e-4 (normwise per output row), independent of the launch options.
+ *
+ *   q      fp32 [heads][group][head_dim].
+ *   k, v   binary16; 16-byte aligned, strides multiples of 8 elements.
+ *   out    fp32 [heads][group][head_dim]; must not overlap the inputs.
+ *   ws     device workspace of ws_bytes >= wsw_attn_decode_workspace_bytes(depth,
+ *          heads, group) bytes, 16-byte aligned, overwritten (WSW_ERR_WORKSPACE
+ *          otherwise).  Two calls in flight at once need two workspaces.
+ *   depth >= 1;  group in {1, 2, 4, 8};  head_dim == 128;  heads <= 65535
+ *   (WSW_ERR_UNSUPPORTED otherwise).
+ * Two launches: chunks of positions in parallel, then their combination (PDL-linked).
+ */
+size_t wsw_attn_decode_workspace_bytes(int64_t depth, int64_t heads, int64_t group);
+int wsw_attn_decode_f16(const float *q, const uint16_t *k, const uint16_t *v, int64_t depth,
+                        int64_t heads, int64_t group, int64_t head_dim, int64_t k_pos_stride,
+                        int64_t k_head_stride, int64_t v_pos_stride, int64_t v_head_stride,
+                        float scale, float *out, void *ws, size_t ws_bytes, void *stream,
                         const wsw_launch_opts *opts);
 
 /*

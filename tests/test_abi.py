@@ -37,10 +37,11 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert wsw.abi_version() == 4
+    assert wsw.abi_version() == 5
     assert wsw.status_string(0) == "WSW_OK"
     assert wsw.status_string(1) == "WSW_ERR_INVALID_ARG"
     assert wsw.status_string(2) == "WSW_ERR_MISALIGNED"
+    assert wsw.status_string(4) == "WSW_ERR_WORKSPACE"
     assert wsw.status_string(99) == "WSW_ERR_UNKNOWN"
 
 
@@ -116,6 +117,23 @@ def test_other_calls_reject_on_host(lib):
     c = lib.wsw_gemv_bf16_chain
     assert c(-1, None, None, None) == INVALID
     assert c(0, None, None, None) == 0
+    ab = lib.wsw_attn_decode_workspace_bytes
+    # one partial (max, sum, 128 values) per (chunk, head, query); chunks of whole
+    # 64-position tiles, about 320 of them over all heads
+    assert ab(32768, 4, 8) == 74 * 4 * 8 * 130 * 4
+    assert ab(1, 4, 1) == 4 * 130 * 4
+    assert ab(0, 4, 1) == 0 and ab(64, 4, 16) == 0
+    a = lib.wsw_attn_decode_f16
+    A = P(4096)
+    def att(depth=64, heads=4, group=8, hd=128, kps=128, khs=8192, vps=128, vhs=8192, k=A, ws=A, wsn=1 << 20):
+        return a(A, k, A, depth, heads, group, hd, kps, khs, vps, vhs, ctypes.c_float(0.1), A, ws, wsn, None, None)
+    assert att(depth=0) == INVALID
+    assert att(ws=None) == INVALID
+    assert att(group=3) == UNSUPPORTED
+    assert att(hd=64) == UNSUPPORTED
+    assert att(kps=132) == MISALIGNED
+    assert att(k=P(4104)) == MISALIGNED
+    assert att(wsn=100) == 4  # WSW_ERR_WORKSPACE
     b = lib.wsw_bounded_wait_check
     assert b(2, P(4096), None) == INVALID
     assert b(0, None, None) == INVALID

@@ -108,6 +108,7 @@ extern "C" const char *wsw_status_string(int status) {
         case WSW_ERR_INVALID_ARG: return "WSW_ERR_INVALID_ARG";
         case WSW_ERR_MISALIGNED: return "WSW_ERR_MISALIGNED";
         case WSW_ERR_UNSUPPORTED: return "WSW_ERR_UNSUPPORTED";
+        case WSW_ERR_WORKSPACE: return "WSW_ERR_WORKSPACE";
         case WSW_ERR_CUDA: return "WSW_ERR_CUDA";
         case WSW_ERR_TIMEOUT: return "WSW_ERR_TIMEOUT";
         default: return "WSW_ERR_UNKNOWN";
