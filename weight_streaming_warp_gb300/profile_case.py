@@ -7,6 +7,7 @@
     python -m weight_streaming_warp_gb300.profile_case dequant_kv [depth]
     python -m weight_streaming_warp_gb300.profile_case moe [T]
     python -m weight_streaming_warp_gb300.profile_case quantize [n block]
+    python -m weight_streaming_warp_gb300.profile_case attn_decode [depth group]
 
 Weights rotate over copies that together exceed the 129 MB L2, so every profiled
 launch streams its weights from HBM; the device holds at most a few GB.  Inputs are
@@ -73,6 +74,15 @@ def main(argv):
         xd = torch.rand((T * 8, K // 32), device=dev, generator=g).half()
         for _ in range(launches):
             wsw.moe_gemv_q8_0(Wq, Wd, xq, xd, ids)
+    elif what == "attn_decode":
+        D = int(argv[1]) if len(argv) > 1 else 32768
+        G = int(argv[2]) if len(argv) > 2 else 1
+        nc = 3  # 3 x 67 MB of K and V at depth 32768
+        K = [torch.randn((4, D, 128), device=dev, generator=g).half() for _ in range(nc)]
+        V = [torch.randn((4, D, 128), device=dev, generator=g).half() for _ in range(nc)]
+        q = torch.randn((4, G, 128), device=dev, generator=g)
+        for i in range(launches):
+            wsw.attn_decode_f16(q, K[i % nc], V[i % nc])
     elif what == "quantize":
         n = int(argv[1]) if len(argv) > 1 else 4096
         block = int(argv[2]) if len(argv) > 2 else 32
