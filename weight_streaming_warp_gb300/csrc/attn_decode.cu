@@ -14,16 +14,17 @@
 //  * attn_decode_split_kernel: grid (splits, heads), 256 threads, two CTAs per SM.  A
 //    CTA takes a chunk of positions of one KV head for all G query heads of its group,
 //    so every K and V byte is read once per step.  Tiles of 64 positions of K and V
-//    (2 x 16 KB) are copied with 16-byte cp.async into a two-stage ring, rows padded to
-//    320 bytes so that the per-position reads below hit distinct banks.
+//    (2 x 16 KB) are copied with 16-byte cp.async into a three-stage ring (two tiles in
+//    flight while one is used); the 16-byte chunks of odd rows are XOR-swizzled so that
+//    the reads below hit distinct banks.
 //      scores:  four lanes per position, each a quarter of the 128 dimensions, for all
 //               G queries at once (each K value is read from shared memory once),
 //               reduced with two xor shuffles; scores are kept in the log2 domain
 //               (scale * log2 e folded into q), so the weights are exp2f(s - m)
 //      softmax: warp g takes query g's 64 scores, the running maximum and the factor
 //               exp2f(m_old - m_new) that rescales what was accumulated so far
-//      values:  warp w takes query w / (8 / G) and every (8 / G)-th position; a lane
-//               owns four dimensions, so a warp reads whole 256-byte V rows
+//      values:  warp w takes every eighth position (w, w + 8, ...) for all G queries;
+//               a lane owns four dimensions, so a warp reads whole 256-byte V rows
 //    At the end of its chunk the CTA adds its warps' partial sums and writes
 //    (m, l = sum of weights, acc[128]) of each query to the workspace.
 //  * attn_decode_combine_kernel (PDL-linked): one CTA per (head, query); rescales every
@@ -96,9 +97,10 @@ __device__ __forceinline__ uint64_t h2_to_f2(uint32_t h) {
 }
 
 // Byte offset of 16-byte chunk c (0..15) of row r in a tile: bit 2 of the chunk index
-// flips on odd rows, so that the score pass (two rows, four chunks a quarter-warp) and
-// the value pass (one row, four chunks a quarter-warp) both read eight distinct chunks
-// of every 128 bytes, i.e. distinct banks.
+// flips on odd rows.  The score pass reads 16-byte chunks, a quarter-warp at a time: two
+// rows, four chunks each, which land on eight distinct chunk positions of 128 bytes,
+// i.e. distinct banks.  The value pass reads 8 bytes a lane, a half-warp at a time: one
+// row's 128 bytes, whose chunks the swizzle only permutes.
 __device__ __forceinline__ int chunk_off(int r, int c) { return r * kRowBytes + ((c ^ ((r & 1) << 2)) << 4); }
 
 template <int G>
