@@ -60,6 +60,8 @@ B_TOKEN_2L = B_Q32 + B_GEMV + B_Q256_Y + B_Q256_X          # quantizer as its ow
 B_FUSED = B_GEMV - K - (K // 32) * 2 + K * 4 + K + (K // 32) * 2  # x in, q and d out, no re-read
 B_TOKEN = B_FUSED + B_Q256_Y + B_Q256_X
 
+WORKLOAD = ("q8_0 decode GEMV 14336x4096 batch 1 + q8_0 quantizer (n=4096, fused into the GEMV launch) "
+            "+ superblock quantizer (n=4096, n=14336), PDL-linked")
 CHAIN_LAYER = [(6144, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
 CHAIN_HEAD = (152064, 5120)
 
@@ -656,10 +658,11 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int8 x int8 -> int32 blocks, fp32 scale/accumulate (q8_0); fp32 quantizer",
+        "dtype": "int8",
         "data": "synthetic: seeded N(0,0.02) bf16 weights quantized to q8_0, N(0,1) activations",
-        "config": {"workload": "q8_0 decode GEMV 14336x4096 batch 1 + q8_0 quantizer (n=4096, fused into "
-                               "the GEMV launch) + superblock quantizer (n=4096, n=14336), PDL-linked",
+        "config": {"workload": WORKLOAD,
+                   "arithmetic": "int8 x int8 -> exact int32 block sums, fp32 scales and accumulation; "
+                                 "fp32 quantizer",
                    "tokens_per_step": TOKENS, "bytes_per_token": B_TOKEN,
                    "weight_copies": NCOPY, "weight_bytes_per_copy": B_GEMV - K - (K // 32) * 2 - M * 4,
                    "l2": "inputs larger than L2: 16 rotating weight copies (1.0 GB) vs 129 MB L2",
@@ -712,8 +715,9 @@ def run_reference(args):
         "impl": "reference",
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp64 oracle",
-        "data": "synthetic", "config": {"workload": "q8_0 decode GEMV 14336x4096 batch 1 + quantizers (one token per step)"},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "arithmetic": "fp64 oracle",
+                                        "sample": "one token per step"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": "one full token per step (all 14336 rows)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
