@@ -31,7 +31,8 @@
  *   - "round" is round-half-away-from-zero (C roundf);
  *   - x / d divides by the fp32 d (the stored fp16 copy of d is only storage);
  *   - both divisions are IEEE fp32 divisions (no reciprocal multiply);
- *   - an all-zero block stores d = +0 and q = 0;
+ *   - an all-zero block stores d = +0 and q = 0, and so does a block whose
+ *     d = amax / 127 rounds to +0 (amax of a few subnormal steps);
  *   - q is clamped to [-127, 127] (a no-op for finite inputs);
  *   - the superblock keeps an fp32 positive scale from amax; the signed "mx" value
  *     that the [P3] excerpt also tracks is not used by any result here;
@@ -154,7 +155,10 @@ int orc_quantize_q8(const float *x, int64_t rows, int64_t n, int64_t ldx, int bl
             float d = amax / 127.0f; /* IEEE fp32 division */
             for (int i = 0; i < block; ++i) {
                 int v = 0;
-                if (amax != 0.0f) {
+                /* d == 0: an all-zero block, or one whose amax is so small (at most
+                 * 63.5 binary32 subnormal steps) that amax / 127 rounds to +0; x / d
+                 * is then undefined and the block is stored as zero. */
+                if (d != 0.0f) {
                     float t = roundf(xb[i] / d); /* fp32 division, half away from zero */
                     if (t > 127.0f)
                         t = 127.0f;

@@ -109,6 +109,32 @@ def test_quantize_all_zero_block(orc):
 
 
 @pytest.mark.parametrize("block", [32, 256])
+def test_quantize_subnormal_blocks(orc, block):
+    """Blocks of binary32 subnormals, where d = fl(amax / 127) reaches the bottom of the
+    range.  s = 2^-149 is the smallest subnormal.  amax = 63 s: amax / 127 < s / 2
+    rounds to +0, and the block is stored as zero (x / 0 is undefined).  amax = 127 s:
+    d = s exactly and q = x / s exactly.  amax = 64 s: amax / 127 is just above s / 2
+    and rounds to d = s, so q = x / s (the amax value itself gives 64, not 127)."""
+    s = np.float32(2.0 ** -149)
+    rng = np.random.default_rng(11)
+    for amax_steps, d_steps in ((63, 0), (127, 1), (64, 1)):
+        k = rng.integers(-amax_steps, amax_steps + 1, size=block)
+        k[rng.integers(block)] = -amax_steps if rng.integers(2) else amax_steps
+        x = (k.astype(np.float32) * s).astype(np.float32)[None, :]
+        assert (x[0] / s == k).all()  # the inputs are exact subnormal multiples
+        q, d = orc.quantize_q8(x, block)
+        if d_steps == 0:
+            assert not q.any()
+            assert (d == 0).all() and not np.signbit(d.astype(np.float32)).any()
+        else:
+            assert (q[0].astype(np.int64) == k).all()
+            if block == 32:
+                assert int(d[0, 0]) == 0  # binary16 has no subnormal this small: +0
+            else:
+                assert d[0, 0] == s
+
+
+@pytest.mark.parametrize("block", [32, 256])
 def test_quantize_single_nonzero(orc, block):
     for v in (1.0, -3.7, 1e-3, 250.0):
         for pos in (0, 5, block - 1):
