@@ -141,3 +141,32 @@ def test_quantize_empty_inputs():
     assert q.numel() == 0
     with pytest.raises(wsw.WswError):
         wsw.quantize_q8(torch.zeros(48, device="cuda"), 32)
+
+
+@pytest.mark.parametrize("block", [32, 256])
+def test_quantize_subnormal_blocks(orc, block):
+    """Blocks of binary32 subnormals: an amax of 63 smallest steps makes amax / 127
+    round to +0 (the block is stored as zero), 64 and 127 steps give d = 2^-149, and
+    blocks of larger subnormals and of normal values sit beside them.  Bit-exact
+    against the oracle, through the standalone quantizer and the fused mat-vec."""
+    wsw = need_gpu()
+    s = 2.0 ** -149
+    rng = np.random.default_rng(5)
+    rows = []
+    for steps in (63, 64, 127, 1000, 2 ** 22, 2 ** 30):
+        k = rng.integers(-min(steps, 2 ** 24), min(steps, 2 ** 24) + 1, size=block).astype(np.float64)
+        k[rng.integers(block)] = steps
+        rows.append((k * s).astype(np.float32))
+    rows.append(np.zeros(block, np.float32))
+    x = torch.from_numpy(np.concatenate(rows)[None, :])
+    _compare(wsw, orc, x, block)
+    if block == 32:
+        K = x.shape[1]
+        Wq = torch.ones((4, K), dtype=torch.int8, device="cuda")
+        Wd = torch.ones((4, K // 32), dtype=torch.float16, device="cuda")
+        xq = torch.empty(K, dtype=torch.int8, device="cuda")
+        xd = torch.empty(K // 32, dtype=torch.float16, device="cuda")
+        wsw.quantize_gemv_q8_0(Wq, Wd, x[0].cuda(), x_out=(xq, xd))
+        torch.cuda.synchronize()
+        qr, sr = orc.quantize_q8(x.numpy(), 32)
+        assert (xq.cpu().numpy() == qr[0]).all() and (f16_bits(xd) == sr[0]).all()

@@ -9,7 +9,8 @@
 //
 // Per block: amax = max |x|; d = amax / 127 (IEEE fp32 division);
 // q = round-half-away(x / d) (IEEE fp32 division by the fp32 d, then roundf),
-// clamped to [-127, 127]; an all-zero block has d = +0 and q = 0.
+// clamped to [-127, 127]; a block whose d is +0 (all zero, or an amax of at most
+// 63.5 subnormal steps, so that amax / 127 rounds to +0) has q = 0.
 #pragma once
 
 #include "common.cuh"
@@ -50,7 +51,7 @@ __device__ __forceinline__ int code_exact(float v, float d) {
 // reciprocal is not a normal finite number takes the exact path for every value.
 __device__ __forceinline__ void codes(const float (&v)[8], float amax, float d, uint32_t (&packed)[2]) {
     packed[0] = packed[1] = 0u;
-    if (amax == 0.0f) return;
+    if (d == 0.0f) return;  // x / d undefined: the block is stored as zero
     const float r = __frcp_rn(d);
     const bool fast = d >= 1.0e-37f && d <= 1.0e37f;
 #pragma unroll
