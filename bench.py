@@ -18,14 +18,20 @@ activation x (length 4096, N(0,1)) quantized to q8_0 in front of it, and the
   value  = algorithmic bytes of the step / step time (GB/s), summed over ranks.
 
 The same line also reports: the fused quantize + GEMV kernel against the HBM roofline
-(CUDA events over back-to-back launches on distinct weight copies), the GEMV alone, the batch-1 quantizer
-in us/call (graph-amortised over 1000 calls), the 27B-shaped bf16 decode chain
-(64 layers x [QKV, O, gate/up, down] + lm_head, 257 PDL-linked mat-vecs, 43.16 GB
-per token), the end-to-end rate through the C ABI with host buffers, and the CPU
-oracle's rate on a bounded sample.
+(CUDA events over back-to-back launches on distinct weight copies), the GEMV alone, the
+other hot-path calls on their configured shapes ("rows": prefill GEMM, KV dequant, decode
+attention, each grouped MoE call and its quantizer), each as plain back-to-back launches,
+PDL-linked, and where one copy fits in L2 also L2-hot (one copy repeated, labelled
+"l2hot"), the end-to-end rate through the C ABI with host buffers, the CPU oracle on a
+bounded sample (all host cores, rows cut over threads, and one core), the 27B-shaped
+bf16 decode chain (64 layers x [QKV, O, gate/up, down] + lm_head, 257 PDL-linked
+mat-vecs, 43.16 GB per token), the batch-1 bf16 4096 x 4096 GEMV, the MoE step
+(quantize -> grouped gate_up -> quantize -> grouped down at T = 1, 16, 512), and last a
+compact "key_numbers" summary.
 
---impl reference times the CPU oracle (the plain single-threaded C restatement) on
-the same workload, one token per step.
+--impl reference times the CPU oracle (the plain C restatement) on the same workload,
+one token per step, its GEMV rows cut over the host cores.
+--profile-case CASE runs one call a few times for a profiler (see profile_case).
 """
 from __future__ import annotations
 
@@ -60,8 +66,7 @@ B_TOKEN_2L = B_Q32 + B_GEMV + B_Q256_Y + B_Q256_X          # quantizer as its ow
 B_FUSED = B_GEMV - K - (K // 32) * 2 + K * 4 + K + (K // 32) * 2  # x in, q and d out, no re-read
 B_TOKEN = B_FUSED + B_Q256_Y + B_Q256_X
 
-WORKLOAD = ("q8_0 decode GEMV 14336x4096 batch 1 + q8_0 quantizer (n=4096, fused into the GEMV launch) "
-            "+ superblock quantizer (n=4096, n=14336), PDL-linked")
+WORKLOAD = "q8_0 decode GEMV 14336x4096 batch 1 + fused q8_0 quantizer n=4096 + superblock quantizer n=4096/14336"
 CHAIN_LAYER = [(6144, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
 CHAIN_HEAD = (152064, 5120)
 
@@ -387,20 +392,60 @@ def _graph_rate(torch, fn, n, reps=5):
     return statistics.median(_time_graph(torch, g, 1) for _ in range(reps)) / n
 
 
-def _rate_both(torch, make_fn, n):
-    """Seconds per call of back-to-back calls in a graph, plain and PDL-linked."""
-    return _graph_rate(torch, make_fn(0), n), _graph_rate(torch, make_fn(1), n)
+def _rates(torch, make, n, hot=True):
+    """Seconds per call of back-to-back calls in a graph: plain and PDL-linked, both
+    rotating over copies larger than L2, and (hot) PDL-linked on one copy, L2-hot."""
+    t = _graph_rate(torch, make(0, False), n)
+    tp = _graph_rate(torch, make(1, False), n)
+    th = _graph_rate(torch, make(1, True), n) if hot else None
+    return t, tp, th
 
 
-def measure_rows(torch, wsw, dev):
-    """The other hot-path calls on their configured shapes (graph-amortised, inputs
-    rotating over copies larger than L2 where a single copy would fit).  Each is timed
-    as plain back-to-back launches ("us") and PDL-linked ones ("us_pdl")."""
-    import weight_streaming_warp_gb300.synthetic as syn
+def _entry(nbytes, t, tp, th=None, flops=None, **extra):
+    """One bench row: us and GB/s (algorithmic bytes) per regime."""
+    e = {"us": round(t * 1e6, 2), "GBps": round(nbytes / t / 1e9, 1),
+         "us_pdl": round(tp * 1e6, 2), "GBps_pdl": round(nbytes / tp / 1e9, 1)}
+    if flops:
+        e["TFLOPs"] = round(flops / t / 1e12, 2)
+        e["TFLOPs_pdl"] = round(flops / tp / 1e12, 2)
+    if th is not None:
+        e["us_l2hot"] = round(th * 1e6, 2)
+        e["GBps_l2hot"] = round(nbytes / th / 1e9, 1)
+        if flops:
+            e["TFLOPs_l2hot"] = round(flops / th / 1e12, 2)
+    e["bytes"] = nbytes
+    e.update(extra)
+    return e
+
+
+def measure_config1(torch, wsw, dev):
+    """The batch-1 bf16 decode GEMV, W 4096 x 4096 (33.6 MB): 32 rotating copies
+    (1.07 GB) plain and PDL-linked, and one copy repeated (L2-hot)."""
+    Mc, Kc, ncp = 4096, 4096, 32
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    Ws = [torch.randn((Mc, Kc), generator=g, device=dev).mul_(0.02).to(torch.bfloat16) for _ in range(ncp)]
+    X = torch.randn((64, Kc), generator=g, device=dev)
+    Y = torch.empty((64, Mc), dtype=torch.float32, device=dev)
+    it = [0]
+
+    def make(pdl, hot):
+        def fn(stream):
+            i = it[0]
+            it[0] += 1
+            wsw.gemv_bf16(Ws[0 if hot else i % ncp], X[i % 64], out=Y[i % 64], opts={"pdl": pdl})
+        return fn
+    t, tp, th = _rates(torch, make, 256)
+    nb = Mc * Kc * 2 + Kc * 4 + Mc * 4
+    del Ws
+    torch.cuda.empty_cache()
+    return _entry(nb, t, tp, th, note="bf16 4096x4096; rotating copies 1.07 GB; l2hot = one copy repeated")
+
+
+def measure_gemm(torch, wsw, dev, out):
+    """Small-batch prefill GEMM, W 2560 x 10240 (packed and one-line padded rows)."""
     g = torch.Generator(device=dev)
     g.manual_seed(2)
-    out = {}
-    # small-batch prefill GEMM, W 2560 x 10240 (packed and one-line padded rows)
     Mg, Kg = 2560, 10240
     Ws = [torch.randn((Mg, Kg), generator=g, device=dev).mul_(0.02).to(torch.bfloat16) for _ in range(12)]
     for ld in (Kg, Kg + 64):
@@ -410,41 +455,50 @@ def measure_rows(torch, wsw, dev):
             Y = torch.empty((N, Mg), dtype=torch.float32, device=dev)
             it = [0]
 
-            def make(pdl, X=X, Y=Y, Wl=Wl):
+            def make(pdl, hot, X=X, Y=Y, Wl=Wl):
                 def fn(stream):
-                    wsw.gemm_bf16(Wl[it[0] % len(Wl)], X, out=Y, opts={"pdl": pdl})
+                    wsw.gemm_bf16(Wl[0 if hot else it[0] % len(Wl)], X, out=Y, opts={"pdl": pdl})
                     it[0] += 1
                 return fn
-            t, tp = _rate_both(torch, make, 24)
+            t, tp, th = _rates(torch, make, 24, hot=(ld == Kg))
             key = "gemm_bf16_N%d_%s" % (N, "packed" if ld == Kg else "padded")
-            nbytes = Mg * Kg * 2 + N * Kg * 2 + N * Mg * 4
-            out[key] = {"us": round(t * 1e6, 2), "TFLOPs": round(2.0 * N * Mg * Kg / t / 1e12, 2),
-                        "GBps": round(nbytes / t / 1e9, 1), "us_pdl": round(tp * 1e6, 2),
-                        "TFLOPs_pdl": round(2.0 * N * Mg * Kg / tp / 1e12, 2), "GBps_pdl": round(nbytes / tp / 1e9, 1)}
+            out[key] = _entry(Mg * Kg * 2 + N * Kg * 2 + N * Mg * 4, t, tp, th, flops=2.0 * N * Mg * Kg)
         del Wl
     del Ws
-    # q8_0 KV cache dequant, 4 heads x 128
+    torch.cuda.empty_cache()
+
+
+def measure_dequant(torch, wsw, dev, out):
+    """q8_0 KV cache dequant, 4 heads x 128, 8 rotating copies."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(4)
     for depth in (32768, 65536):
         copies = 8
-        qs = [torch.randint(-127, 128, (depth, 4, 128), dtype=torch.int8, device=dev, generator=g) for _ in range(copies)]
+        qs = [torch.randint(-127, 128, (depth, 4, 128), dtype=torch.int8, device=dev, generator=g)
+              for _ in range(copies)]
         ds = [torch.rand((depth, 4, 4), device=dev, generator=g).half() for _ in range(copies)]
         o = torch.empty((4, depth, 128), dtype=torch.float16, device=dev)
         it = [0]
 
-        def make(pdl, qs=qs, ds=ds, o=o):
+        def make(pdl, hot, qs=qs, ds=ds, o=o):
             def fn(stream):
-                i = it[0] % copies
+                i = 0 if hot else it[0] % copies
                 wsw.dequant_q8_0_kv(qs[i], ds[i], out=o, opts={"pdl": pdl})
                 it[0] += 1
             return fn
-        t, tp = _rate_both(torch, make, 32)
+        t, tp, th = _rates(torch, make, 32)
         nb = depth * 4 * 128 * (1 + 2) + depth * 4 * 4 * 2
-        out["dequant_kv_d%d" % depth] = {"us": round(t * 1e6, 2), "GBps": round(nb / t / 1e9, 1),
-                                         "us_pdl": round(tp * 1e6, 2), "GBps_pdl": round(nb / tp / 1e9, 1)}
+        out["dequant_kv_d%d" % depth] = _entry(nb, t, tp, th)
         del qs, ds
-    # decode attention over the binary16 KV (4 KV heads x 128; groups of 1 and 8 query
-    # heads), reading the per-head scratch and the position-major cache; 4 copies of K
-    # and V rotate (268 MB and more)
+    torch.cuda.empty_cache()
+
+
+def measure_attn_decode(torch, wsw, dev, out):
+    """Decode attention over the binary16 KV (4 KV heads x 128; groups of 1 and 8
+    query heads), reading the per-head scratch and the position-major cache; 4 copies
+    of K and V rotate (268 MB and more)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
     for depth in (32768, 65536):
         copies = 4
         Ks = [torch.randn((4, depth, 128), generator=g, device=dev).half() for _ in range(copies)]
@@ -458,9 +512,9 @@ def measure_rows(torch, wsw, dev):
             for layout in ("per_head", "position_major"):
                 it = [0]
 
-                def make(pdl, qq=qq, o=o, ws=ws, layout=layout, it=it):
+                def make(pdl, hot, qq=qq, o=o, ws=ws, layout=layout, it=it):
                     def fn(stream):
-                        i = it[0] % copies
+                        i = 0 if hot else it[0] % copies
                         it[0] += 1
                         if layout == "per_head":
                             k, v = Ks[i], Vs[i]
@@ -468,46 +522,114 @@ def measure_rows(torch, wsw, dev):
                             k, v = Kc[i].permute(1, 0, 2), Vc[i].permute(1, 0, 2)
                         wsw.attn_decode_f16(qq, k, v, out=o, ws=ws, opts={"pdl": pdl})
                     return fn
-                t, tp = _rate_both(torch, make, 32)
+                t, tp, th = _rates(torch, make, 32, hot=(layout == "per_head"))
                 nb = 2 * depth * 4 * 128 * 2 + 2 * 4 * group * 128 * 4
-                out["attn_decode_d%d_g%d_%s" % (depth, group, layout)] = {
-                    "us": round(t * 1e6, 2), "GBps": round(nb / t / 1e9, 1),
-                    "us_pdl": round(tp * 1e6, 2), "GBps_pdl": round(nb / tp / 1e9, 1)}
+                out["attn_decode_d%d_g%d_%s" % (depth, group, layout)] = _entry(nb, t, tp, th)
         del Ks, Vs, Kc, Vc
-    # grouped MoE mat-vec (gate_up: 1536 x 2048 per expert), 128 experts, top-8; calls
-    # rotate over 8 routings and 2 copies of the expert weights (2 x 403 MB), so the
-    # experts a call reads are not left in L2 by the call before
-    E, Mo, Km = 128, 1536, 2048
+    torch.cuda.empty_cache()
+
+
+MOE_E, MOE_H, MOE_F, MOE_TOPK = 128, 2048, 768, 8
+
+
+def _moe_bytes(used, Mo, Kx, R):
+    """Algorithmic bytes of one grouped call: the used experts' q8_0 rows once, the
+    q8_0 activations, y."""
+    return int(used * (Mo * Kx + Mo * Kx // 16) + R * (Kx + Kx // 16) + R * Mo * 4)
+
+
+def _quant_bytes(R, n):
+    return R * n * 4 + R * n + R * (n // 32) * 2
+
+
+def measure_moe(torch, wsw, dev, out):
+    """The MoE step of 128 experts, top-8, hidden 2048, expert FFN 768: per T the
+    activations (R = 8 T rows, N(0,1)) are quantized per row (q8_0), the grouped
+    gate_up mat-vec (1536 x 2048 per expert) runs, the down input (R x 768, N(0,1),
+    standing in for the SwiGLU output) is quantized and the grouped down mat-vec
+    (2048 x 768 per expert) runs.  Calls rotate over 8 routings and 2 copies of the
+    expert weights (2 x 428 MB gate_up, 2 x 214 MB down), so the experts a call reads
+    are not left in L2 by the call before.  Reports the whole step, each grouped call,
+    and (T = 1 and 16, whose experts fit in L2) the same calls repeated on one routing
+    and one copy (L2-hot)."""
+    import weight_streaming_warp_gb300.synthetic as syn
+    g = torch.Generator(device=dev)
+    g.manual_seed(6)
+    E, H, F = MOE_E, MOE_H, MOE_F
     nw, nr = 2, 8
-    Wqs = [torch.randint(-127, 128, (E, Mo, Km), dtype=torch.int8, device=dev, generator=g) for _ in range(nw)]
-    Wds = [(torch.rand((E, Mo, Km // 32), device=dev, generator=g) * 1e-3).half() for _ in range(nw)]
+
+    def qweights(Mo, Kx):
+        return [(torch.randint(-127, 128, (E, Mo, Kx), dtype=torch.int8, device=dev, generator=g),
+                 (torch.rand((E, Mo, Kx // 32), device=dev, generator=g) * 1e-3).half()) for _ in range(nw)]
+    Wg, Wdn = qweights(2 * F, H), qweights(H, F)
+    steps = {}
     for T in (1, 16, 512):
-        R = T * 8
-        idss = [syn.routing(r, "bench_route%d" % T, T, E, 8).to(dev) for r in range(nr)]
-        xq = torch.randint(-127, 128, (R, Km), dtype=torch.int8, device=dev, generator=g)
-        xd = torch.rand((R, Km // 32), device=dev, generator=g).half()
-        y = torch.empty((R, Mo), dtype=torch.float32, device=dev)
-        nws = wsw.moe_workspace_bytes(E, Km, R)
+        R = T * MOE_TOPK
+        idss = [syn.routing(r, "bench_route%d" % T, T, E, MOE_TOPK).to(dev) for r in range(nr)]
+        xs = [torch.randn((R, H), generator=g, device=dev) for _ in range(2)]
+        hs = [torch.randn((R, F), generator=g, device=dev) for _ in range(2)]
+        xq = torch.empty((R, H), dtype=torch.int8, device=dev)
+        xd = torch.empty((R, H // 32), dtype=torch.float16, device=dev)
+        hq = torch.empty((R, F), dtype=torch.int8, device=dev)
+        hd = torch.empty((R, F // 32), dtype=torch.float16, device=dev)
+        yg = torch.empty((R, 2 * F), dtype=torch.float32, device=dev)
+        yd = torch.empty((R, H), dtype=torch.float32, device=dev)
+        nws = max(wsw.moe_workspace_bytes(E, H, R), wsw.moe_workspace_bytes(E, F, R))
         ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else False
+        used = statistics.mean(len(set(ids.tolist())) for ids in idss)
         it = [0]
 
-        def make(pdl, idss=idss, xq=xq, xd=xd, y=y, it=it, ws=ws):
+        def part(which, pdl, hot):
             def fn(stream):
-                i = it[0]
+                i = 0 if hot else it[0]
                 it[0] += 1
-                wsw.moe_gemv_q8_0(Wqs[i % nw], Wds[i % nw], xq, xd, idss[i % nr], out=y, opts={"pdl": pdl},
-                                  ws=ws)
+                o = {"pdl": pdl}
+                ids = idss[i % nr]
+                if which in ("step", "quant_gate_up"):
+                    wsw.quantize_q8(xs[i % 2], 32, out=(xq, xd), opts=o)
+                if which in ("step", "gate_up"):
+                    Wq, Wd = Wg[i % nw]
+                    wsw.moe_gemv_q8_0(Wq, Wd, xq, xd, ids, out=yg, opts=o, ws=ws)
+                if which in ("step", "quant_down"):
+                    wsw.quantize_q8(hs[i % 2], 32, out=(hq, hd), opts=o)
+                if which in ("step", "down"):
+                    Wq, Wd = Wdn[i % nw]
+                    wsw.moe_gemv_q8_0(Wq, Wd, hq, hd, ids, out=yd, opts=o, ws=ws)
             return fn
-        t, tp = _rate_both(torch, make, 8 if T == 512 else 32)
-        used = statistics.mean(len(set(ids.tolist())) for ids in idss)
-        nb = used * (Mo * Km + Mo * Km // 16) + R * (Km + Km // 16) + R * Mo * 4
-        out["moe_gate_up_T%d" % T] = {"us": round(t * 1e6, 2), "experts_used": used, "GBps": round(nb / t / 1e9, 1),
-                                     "us_pdl": round(tp * 1e6, 2), "GBps_pdl": round(nb / tp / 1e9, 1),
-                                     "note": "weights of the used experts once + activations + y; "
-                                             "8 routings x 2 weight copies rotate"}
-    del Wqs, Wds
+        n = 8 if T == 512 else 32
+        hot = T <= 16
+        b_qg, b_qd = _quant_bytes(R, H), _quant_bytes(R, F)
+        b_g, b_d = _moe_bytes(used, 2 * F, H, R), _moe_bytes(used, H, F, R)
+        t, tp, th = _rates(torch, lambda pdl, h: part("step", pdl, h), n, hot=hot)
+        steps[T] = _entry(b_qg + b_g + b_qd + b_d, t, tp, th, experts_used=used,
+                          calls="quantize_q8 gate_up input -> moe gate_up -> quantize_q8 down input -> moe down")
+        parts = {}
+        for name, nb in (("quant_gate_up", b_qg), ("gate_up", b_g), ("quant_down", b_qd), ("down", b_d)):
+            tt, ttp, tth = _rates(torch, lambda pdl, h, name=name: part(name, pdl, h), n, hot=hot)
+            parts[name] = _entry(nb, tt, ttp, tth)
+        out["moe_gate_up_T%d" % T] = dict(parts["gate_up"], experts_used=used)
+        out["moe_down_T%d" % T] = dict(parts["down"], experts_used=used)
+        out["moe_quantize_T%d" % T] = {"gate_up_input_us_pdl": parts["quant_gate_up"]["us_pdl"],
+                                       "down_input_us_pdl": parts["quant_down"]["us_pdl"],
+                                       "gate_up_input_GBps_pdl": parts["quant_gate_up"]["GBps_pdl"],
+                                       "down_input_GBps_pdl": parts["quant_down"]["GBps_pdl"]}
+        del xs, hs, ws
+    del Wg, Wdn
     torch.cuda.empty_cache()
-    return out
+    return steps
+
+
+def measure_rows(torch, wsw, dev):
+    """The other hot-path calls on their configured shapes (graph-amortised, inputs
+    rotating over copies larger than L2 where a single copy would fit).  Each is timed
+    as plain back-to-back launches ("us"), PDL-linked ones ("us_pdl") and, where one
+    copy fits in the 129 MB L2, PDL-linked on one copy ("us_l2hot")."""
+    out = {}
+    measure_gemm(torch, wsw, dev, out)
+    measure_dequant(torch, wsw, dev, out)
+    measure_attn_decode(torch, wsw, dev, out)
+    moe_steps = measure_moe(torch, wsw, dev, out)
+    return out, moe_steps
 
 
 def measure_e2e(torch, wl, dev, steps, step_graph=None):
@@ -554,28 +676,52 @@ def _cpu_inputs():
     return _CPU_INPUTS
 
 
-def cpu_oracle_tokens(n):
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_oracle_tokens(n, threads=1):
     """Run n tokens of the workload through the oracle (quantize x, q8_0 GEMV over
-    all 14336 rows, the two superblock quantizations); returns elapsed seconds."""
+    all 14336 rows, the two superblock quantizations); returns elapsed seconds.
+    With threads > 1 the GEMV's rows are cut into `threads` contiguous ranges, each
+    an oracle call on its own host thread (the C oracle runs without the GIL); the
+    oracle's arithmetic per row is unchanged."""
     import numpy as np
     import oracle as orc
     Wq, Wd, X = _cpu_inputs()
+    pool = None
+    if threads > 1:
+        import concurrent.futures as cf
+        pool = cf.ThreadPoolExecutor(max_workers=threads)
+        cuts = [M * i // threads for i in range(threads + 1)]
     t0 = time.perf_counter()
     for i in range(n):
         x = X[i % 8:i % 8 + 1]
         xq, xd = orc.quantize_q8(x, 32)
-        y = orc.gemv_q8_0(Wq, Wd, xq[0], xd[0]).astype(np.float32)
-        orc.quantize_q8(y[None, :], 256)
+        if pool is None:
+            y = orc.gemv_q8_0(Wq, Wd, xq[0], xd[0])
+        else:
+            parts = list(pool.map(lambda j: orc.gemv_q8_0(Wq[cuts[j]:cuts[j + 1]], Wd[cuts[j]:cuts[j + 1]],
+                                                          xq[0], xd[0]), range(threads)))
+            y = np.concatenate(parts)
+        orc.quantize_q8(y.astype(np.float32)[None, :], 256)
         orc.quantize_q8(x, 256)
-    return time.perf_counter() - t0
+    el = time.perf_counter() - t0
+    if pool is not None:
+        pool.shutdown()
+    return el
 
 
-def cpu_oracle_rate(seconds=10.0):
+def cpu_oracle_rate(seconds=10.0, threads=1):
     """GB/s of the oracle over about `seconds` of host time (at least 2 tokens)."""
     _cpu_inputs()
-    per = cpu_oracle_tokens(1)
+    per = cpu_oracle_tokens(1, threads)
     n = max(2, int(seconds / max(per, 1e-6)))
-    el = cpu_oracle_tokens(n)
+    el = cpu_oracle_tokens(n, threads)
     return B_TOKEN * n / el / 1e9, n, el
 
 
@@ -638,7 +784,8 @@ def run_ours(args):
     e2e_eager = measure_e2e(torch, wl, dev, args.steps)
     del step_graph
     chain = measure_chain(torch, wsw, dev) if rank == 0 else None
-    rows = measure_rows(torch, wsw, dev) if rank == 0 else None
+    config1 = measure_config1(torch, wsw, dev) if rank == 0 else None
+    rows, moe_steps = measure_rows(torch, wsw, dev) if rank == 0 else (None, None)
 
     if pg:
         pg.barrier()
@@ -646,7 +793,13 @@ def run_ours(args):
         if pg:
             pg.destroy_process_group()
         return
-    cpu_v, cpu_n, cpu_s = cpu_oracle_rate(seconds=10.0) if world == 1 else (None, 0, 0.0)
+    cores = host_cores()
+    cpu1 = cpu_oracle_rate(seconds=8.0) if world == 1 else None
+    cpuN = cpu_oracle_rate(seconds=8.0, threads=cores) if world == 1 else None
+    if chain is not None:
+        for arm in ("pdl", "no_pdl", "pdl_l2_prefetch_4"):
+            chain[arm]["frac_of_measured"] = round(chain[arm]["GBps"] / peak, 4)
+            chain[arm]["frac_of_nominal_8TBps"] = round(chain[arm]["GBps"] / NOMINAL_HBM_GBS, 4)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -670,11 +823,11 @@ def run_ours(args):
                    "timing": "CUDA events around K replays of a CUDA graph of one step"},
         "pct_of_measured_hbm_peak": round(100.0 * value / world / peak, 2),
         "pct_of_nominal_8TBps": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
-        "quantizer_us_per_call": quant,
         "roofline": {"kernel": "stream_gemv_kernel<Q8X> (quantize_gemv_q8_0)", "bound": "hbm",
                      "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "frac_of_nominal_8TBps": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": _traffic_record("quantize_gemv_q8_0"),
                      "algorithmic_bytes_per_launch": B_FUSED,
                      "launch_us": {"median": round(k_med * 1e6, 3), "min": round(k_min * 1e6, 3),
@@ -685,17 +838,42 @@ def run_ours(args):
         "two_launch_step": {"GBps": round(B_TOKEN_2L * TOKENS / two_s / 1e9, 2),
                             "ms_per_step": round(two_s * 1e3, 4),
                             "note": "quantize_q8 -> gemv_q8_0 as two PDL-linked launches per token"},
-        "chain_27b_bf16": chain,
         "rows": rows,
         "e2e": e2e,
         "e2e_eager": e2e_eager,
         "gpu_launches": 3 * TOKENS * args.steps,
         "clocks": clk,
-        "cpu_baseline": None if cpu_v is None else {
-            "value": round(cpu_v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d full tokens (quantize + 14336x4096 q8_0 GEMV + 2 superblock quantizations) in %.1f s"
-                      % (cpu_n, cpu_s)},
+        "cpu_baseline": None if cpuN is None else {
+            "value": round(cpuN[0], 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d full tokens (quantize + 14336x4096 q8_0 GEMV rows cut over %d host threads + 2 "
+                      "superblock quantizations) in %.1f s" % (cpuN[1], cores, cpuN[2]),
+            "single_core": {"value": round(cpu1[0], 4), "cores": 1,
+                            "sample": "%d full tokens in %.1f s" % (cpu1[1], cpu1[2])}},
+        "chain_27b_bf16": chain,
+        "config1_gemv_bf16_4096x4096": config1,
+        "moe_step": None if moe_steps is None else {"T%d" % T: s for T, s in moe_steps.items()},
     }
+    # The figures a reader needs first, last on the line.
+    if rank == 0:
+        key = {"fused_q8_0_gemv": {"GBps": round(achieved, 1), "frac_measured": round(achieved / peak, 4),
+                                   "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
+               "gemv_q8_0_alone_frac": round(B_GEMV / g_med / 1e9 / peak, 4),
+               "quantizer_us_per_call": quant}
+        if chain is not None:
+            c = chain["pdl"]
+            key["chain_27b_bf16_pdl"] = {"GBps": c["GBps"], "tok_per_s": c["tok_per_s"],
+                                         "frac_measured": c["frac_of_measured"],
+                                         "frac_nominal": c["frac_of_nominal_8TBps"]}
+        if config1 is not None:
+            key["config1_gemv_bf16"] = {"GBps_pdl": config1["GBps_pdl"], "GBps": config1["GBps"],
+                                        "frac_pdl": round(config1["GBps_pdl"] / peak, 4),
+                                        "GBps_l2hot": config1["GBps_l2hot"]}
+        if moe_steps is not None:
+            key["config4_moe_step_us_pdl"] = {"T%d" % T: s["us_pdl"] for T, s in moe_steps.items()}
+            key["config4_moe_step_GBps_pdl"] = {"T%d" % T: s["GBps_pdl"] for T, s in moe_steps.items()}
+        if cpuN is not None:
+            key["cpu_oracle_GBps"] = {"cores_%d" % cores: round(cpuN[0], 3), "cores_1": round(cpu1[0], 3)}
+        line["key_numbers"] = key
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
@@ -708,8 +886,9 @@ def run_reference(args):
     import oracle
     oracle.lib()
     _cpu_inputs()
-    cpu_oracle_tokens(args.warmup)
-    el = cpu_oracle_tokens(args.steps)
+    cores = host_cores()
+    cpu_oracle_tokens(args.warmup, cores)
+    el = cpu_oracle_tokens(args.steps, cores)
     value = B_TOKEN * args.steps / el / 1e9
     line = {
         "impl": "reference",
@@ -718,11 +897,103 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "arithmetic": "fp64 oracle",
                                         "sample": "one token per step"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "one full token per step (all 14336 rows)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "one full token per step (all 14336 rows, cut over %d host threads)" % cores},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------- profile cases --
+def profile_case(argv):
+    """Run one hot-path call on its configured shape a few times, for a profiler:
+
+        python bench.py --profile-case gemv_q8_0
+        python bench.py --profile-case quantize_gemv_q8_0
+        python bench.py --profile-case gemv_bf16 [M K]
+        python bench.py --profile-case gemm_bf16 [N]
+        python bench.py --profile-case dequant_kv [depth]
+        python bench.py --profile-case moe [T [gate_up|down]]
+        python bench.py --profile-case quantize [n block]
+        python bench.py --profile-case attn_decode [depth group]
+
+    Weights rotate over copies that together exceed the 129 MB L2, so every profiled
+    launch streams its weights from HBM; the device holds at most a few GB.  Inputs
+    are random (values do not change the work of these kernels)."""
+    import torch
+    import weight_streaming_warp_gb300 as wsw
+    from weight_streaming_warp_gb300 import build as wbuild
+    wbuild.build()
+    what = argv[0] if argv else "gemv_q8_0"
+    dev = "cuda"
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    launches = 6
+    if what in ("gemv_q8_0", "quantize_gemv_q8_0"):
+        nc = 4
+        Wq = [torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=g) for _ in range(nc)]
+        Wd = [(torch.rand((M, K // 32), device=dev, generator=g) * 1e-3).half() for _ in range(nc)]
+        x = torch.randn((launches, K), device=dev, generator=g)
+        xq = torch.empty(K, dtype=torch.int8, device=dev)
+        xd = torch.empty(K // 32, dtype=torch.float16, device=dev)
+        for i in range(launches):
+            if what == "gemv_q8_0":
+                wsw.gemv_q8_0(Wq[i % nc], Wd[i % nc], xq, xd)
+            else:
+                wsw.quantize_gemv_q8_0(Wq[i % nc], Wd[i % nc], x[i], x_out=(xq, xd))
+    elif what == "gemv_bf16":
+        Mi, Ki = (int(argv[1]), int(argv[2])) if len(argv) > 2 else (5120, 17408)
+        nc = max(2, (512 << 20) // (Mi * Ki * 2) + 1)
+        W = [torch.randn((Mi, Ki), device=dev, generator=g).to(torch.bfloat16) for _ in range(nc)]
+        x = torch.randn(Ki, device=dev, generator=g)
+        for i in range(launches):
+            wsw.gemv_bf16(W[i % nc], x)
+    elif what == "gemm_bf16":
+        N = int(argv[1]) if len(argv) > 1 else 512
+        Mg, Kg, nc = 2560, 10240, 4
+        W = [torch.randn((Mg, Kg), device=dev, generator=g).mul_(0.02).to(torch.bfloat16) for _ in range(nc)]
+        X = torch.randn((N, Kg), device=dev, generator=g).to(torch.bfloat16)
+        for i in range(launches):
+            wsw.gemm_bf16(W[i % nc], X)
+    elif what == "dequant_kv":
+        D = int(argv[1]) if len(argv) > 1 else 65536
+        nc = 4
+        q = [torch.randint(-127, 128, (D, 4, 128), dtype=torch.int8, device=dev, generator=g) for _ in range(nc)]
+        d = [torch.rand((D, 4, 4), device=dev, generator=g).half() for _ in range(nc)]
+        for i in range(launches):
+            wsw.dequant_q8_0_kv(q[i % nc], d[i % nc])
+    elif what == "moe":
+        from weight_streaming_warp_gb300 import synthetic as syn
+        T = int(argv[1]) if len(argv) > 1 else 16
+        down = len(argv) > 2 and argv[2] == "down"
+        E = MOE_E
+        Mo, Kx = (MOE_H, MOE_F) if down else (2 * MOE_F, MOE_H)
+        Wq = torch.randint(-127, 128, (E, Mo, Kx), dtype=torch.int8, device=dev, generator=g)
+        Wd = (torch.rand((E, Mo, Kx // 32), device=dev, generator=g) * 1e-3).half()
+        ids = syn.routing(0, "profile%d" % T, T, E, MOE_TOPK).to(dev)
+        xq = torch.randint(-127, 128, (T * MOE_TOPK, Kx), dtype=torch.int8, device=dev, generator=g)
+        xd = torch.rand((T * MOE_TOPK, Kx // 32), device=dev, generator=g).half()
+        for _ in range(launches):
+            wsw.moe_gemv_q8_0(Wq, Wd, xq, xd, ids)
+    elif what == "attn_decode":
+        D = int(argv[1]) if len(argv) > 1 else 32768
+        G = int(argv[2]) if len(argv) > 2 else 1
+        nc = 3  # 3 x 67 MB of K and V at depth 32768
+        Kt = [torch.randn((4, D, 128), device=dev, generator=g).half() for _ in range(nc)]
+        Vt = [torch.randn((4, D, 128), device=dev, generator=g).half() for _ in range(nc)]
+        q = torch.randn((4, G, 128), device=dev, generator=g)
+        for i in range(launches):
+            wsw.attn_decode_f16(q, Kt[i % nc], Vt[i % nc])
+    elif what == "quantize":
+        n = int(argv[1]) if len(argv) > 1 else 4096
+        block = int(argv[2]) if len(argv) > 2 else 32
+        X = torch.randn((64, n), device=dev, generator=g)
+        for i in range(launches):
+            wsw.quantize_q8(X[i], block)
+    else:
+        raise SystemExit("unknown profile case %r" % what)
+    torch.cuda.synchronize()
+    print("done", what)
 
 
 def main():
@@ -731,7 +1002,12 @@ def main():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--profile-case", nargs="+", metavar="CASE",
+                    help="run one call a few times for a profiler (see profile_case) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args.profile_case)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -27,3 +27,21 @@ def test_reference_arm_prints_the_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_oracle_rows_cut_over_threads_change_no_bit(orc):
+    """The all-core CPU baseline cuts the oracle's GEMV rows over host threads; every
+    row is the same oracle computation, so the result equals one call bit for bit."""
+    import concurrent.futures as cf
+    import numpy as np
+    g = np.random.default_rng(0)
+    M, K, parts = 1001, 512, 7
+    Wq = g.integers(-127, 128, size=(M, K)).astype(np.int8)
+    Wd = g.integers(0x0c00, 0x1800, size=(M, K // 32)).astype(np.uint16)
+    xq = g.integers(-127, 128, size=K).astype(np.int8)
+    xd = g.integers(0x2000, 0x2c00, size=K // 32).astype(np.uint16)
+    cuts = [M * j // parts for j in range(parts + 1)]
+    with cf.ThreadPoolExecutor(max_workers=parts) as pool:
+        y = np.concatenate(list(pool.map(lambda j: orc.gemv_q8_0(Wq[cuts[j]:cuts[j + 1]], Wd[cuts[j]:cuts[j + 1]],
+                                                                 xq, xd), range(parts))))
+    assert (y.view(np.uint64) == orc.gemv_q8_0(Wq, Wd, xq, xd).view(np.uint64)).all()

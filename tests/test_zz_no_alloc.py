@@ -3,7 +3,8 @@ device memory (a plugin interface that receives only its input and output buffer
 runtime whose memory pool is fixed at start-up).  It runs the tensor-core form on the
 library's own scratch array instead of a caller workspace.  Its results are checked
 against wsw_moe_gemv_q8_0 with a workspace on two calls in a row, which share that
-scratch, and sizes beyond the scratch are refused.
+scratch: bit for bit against the workspace form and within the q8_0 tolerance against
+the oracle.  Sizes beyond the scratch are refused.
 
 This file is collected last so that a run that stops at its first failure has run
 every other test before it."""
@@ -41,7 +42,9 @@ def _problem(seed, En, Mo, K, T, topk):
     return Wq, Wd, xq, xd, ids
 
 
-def test_noalloc_matches_the_workspace_form_on_two_calls():
+def test_noalloc_matches_the_workspace_form_on_two_calls(orc):
+    """Both forms run the same deterministic tensor-core kernel, so every valid row is
+    equal bit for bit; each row is also checked against the oracle."""
     wsw = need_gpu()
     f = _noalloc(wsw)
     En, Mo, K, T, topk = 24, 384, 1024, 48, 8  # 384 routed rows: the tensor-core form
@@ -55,21 +58,25 @@ def test_noalloc_matches_the_workspace_form_on_two_calls():
             ids[3] = En  # an out-of-range id: flagged, its row left untouched
         xqd, xdd = torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda()
         idd = torch.from_numpy(ids).cuda()
-        ref = wsw.moe_gemv_q8_0(Wqd, Wdd, xqd, xdd, idd)  # with a caller workspace
+        ref = torch.full((T * topk, Mo), 7.0, device="cuda")
+        wsw.moe_gemv_q8_0(Wqd, Wdd, xqd, xdd, idd, out=ref)  # with a caller workspace
         y = torch.full((T * topk, Mo), 7.0, device="cuda")
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         rc = f(Wqd.data_ptr(), Wdd.data_ptr(), En, Mo, K, xqd.data_ptr(), xdd.data_ptr(), idd.data_ptr(),
                T * topk, y.data_ptr(), err.data_ptr(), stream, None)
         assert rc == 0, wsw.status_string(rc)
         torch.cuda.synchronize()
-        yc, rc_ = y.cpu().numpy(), ref.cpu().numpy()
         assert (err.item() != 0) == (call == 1)
+        assert torch.equal(y.view(torch.int32), ref.view(torch.int32)), "call %d: not bit-identical" % call
+        y64, bad = orc.moe_gemv_q8_0(Wq, Wd, xq, xd, ids, y_init=np.full((T * topk, Mo), 7.0))
+        assert bad == (1 if call == 1 else 0)
+        yc = y.cpu().numpy()
         for m in range(T * topk):
             e = ids[m]
             if e >= En:
                 assert (yc[m] == 7.0).all()
                 continue
-            check_tol(yc[m], rc_[m], mag_q8(Wq[e], Wd[e], xq[m], xd[m]), TOL_Q8, "call %d row %d" % (call, m))
+            check_tol(yc[m], y64[m], mag_q8(Wq[e], Wd[e], xq[m], xd[m]), TOL_Q8, "call %d row %d" % (call, m))
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
