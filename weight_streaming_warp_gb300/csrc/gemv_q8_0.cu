@@ -140,21 +140,25 @@ struct Q8X : Q8 {
     template <bool XS>
     __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
         constexpr int kB = 2;  // passes whose x loads are in flight together
-        const int64_t nslots = static_cast<int64_t>(nsteps) * 32;
+        // 32-bit indices: K <= 2^24 (checked on the host), so every offset fits.
+        const int K = static_cast<int>(a.K);
+        const int nslots = nsteps * 32;
         uint16_t *xs_d = reinterpret_cast<uint16_t *>(xsm + 32 * nslots);
         const bool xvec = (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
         const bool out = blockIdx.x == 0 && a.xq_out != nullptr;
         const bool ovec = (reinterpret_cast<uintptr_t>(a.xq_out) & 7) == 0;
-        const int64_t nt = 4 * nslots;  // a multiple of 128: whole warps iterate together
+        const int nt = 4 * nslots;  // a multiple of 128: whole warps iterate together
+        const int bd = static_cast<int>(blockDim.x);
         // Thread t quantizes values 8t .. 8t+7, quarter (t & 3) of block t >> 2 (block
-        // amax uses shuffles, so every lane of a warp runs every pass).  Blocks past K
+        // amax uses shuffles, so every lane of a warp takes part in a unit or none does:
+        // nt is a multiple of 128 and a warp's 32 units are consecutive).  Blocks past K
         // are zero: d = +0 and q = 0, as the padding of Q8.
-        for (int64_t t0 = threadIdx.x; t0 < nt; t0 += kB * static_cast<int64_t>(blockDim.x)) {
+        for (int t0 = static_cast<int>(threadIdx.x); t0 < nt; t0 += kB * bd) {
             float v[kB][8];
 #pragma unroll
             for (int u = 0; u < kB; ++u) {
-                const int64_t e0 = 8 * (t0 + u * static_cast<int64_t>(blockDim.x));
-                if (e0 < a.K) {  // K % 32 == 0: a block is entirely inside or outside
+                const int e0 = 8 * (t0 + u * bd);
+                if (e0 < K) {  // K % 32 == 0: a block is entirely inside or outside
                     if (xvec) {
                         const float4 p = __ldg(reinterpret_cast<const float4 *>(a.x + e0));
                         const float4 q = __ldg(reinterpret_cast<const float4 *>(a.x + e0) + 1);
@@ -171,20 +175,20 @@ struct Q8X : Q8 {
             }
 #pragma unroll
             for (int u = 0; u < kB; ++u) {
-                const int64_t t = t0 + u * static_cast<int64_t>(blockDim.x);
+                const int t = t0 + u * bd;
+                if (t >= nt) break;  // warp-uniform, and so are the later units
                 const float amax = q8m::block_amax<32>(v[u]);
-                if (t >= nt) continue;  // warp-uniform
                 const float d = q8m::scale(amax);
                 uint32_t p[2];
                 q8m::codes(v[u], amax, d, p);
-                const int64_t b = t >> 2;
-                const int qt = static_cast<int>(t & 3);
+                const int b = t >> 2;
+                const int qt = t & 3;
                 // bytes 8 qt .. 8 qt + 7 of block b: plane qt >> 1, offset 8 (qt & 1)
                 *reinterpret_cast<uint2 *>(xsm + ((qt >> 1) * nslots + b) * 16 + 8 * (qt & 1)) = make_uint2(p[0], p[1]);
                 const uint16_t dbits = __half_as_ushort(__float2half_rn(d));
                 if (qt == 0) xs_d[b] = dbits;
-                const int64_t e0 = 8 * t;
-                if (out && e0 < a.K) {
+                const int e0 = 8 * t;
+                if (out && e0 < K) {
                     if (ovec) {
                         *reinterpret_cast<uint2 *>(a.xq_out + e0) = make_uint2(p[0], p[1]);
                     } else {

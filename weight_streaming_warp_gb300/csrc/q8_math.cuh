@@ -40,32 +40,40 @@ __device__ __forceinline__ int code_exact(float v, float d) {
 
 // The 8 codes of this lane, packed little-endian into two words.
 //
-// Division by d is replaced by a product with r = fl(1/d), exactly.  With the
-// standard model fl(a op b) = (a op b)(1 + e), |e| <= 2^-24, and |v| <= amax so that
+// Division by d is replaced by a product with r = fl(1 / d).  With the standard model
+// fl(a op b) = (a op b)(1 + e), |e| <= 2^-24, and |v| <= amax, so that
 // |v / d| <= 127 (1 + 2^-23): t = fl(v * r) = (v / d)(1 + e1)(1 + e2) lies within
-// |v/d| * 2.0001 * 2^-24 < 1.6e-5 of v / d, and fl(v / d) within 7.6e-6 of it, so
-// t and fl(v / d) differ by less than 2.4e-5 < 2^-15.  Rounding to the nearest
-// integer can then only differ when a half-integer lies within 2^-15 of t; for
-// those (rare) values the quotient is computed exactly.  Away from half-integers
-// round-half-even (one conversion) equals round-half-away.  A scale whose
-// reciprocal is not a normal finite number takes the exact path for every value.
+// |v / d| (2^-23 + 2^-48) < 1.6e-5 of v / d, and fl(v / d) within half an ulp at 128
+// (3.9e-6) of it, so t and fl(v / d) differ by less than 2.0e-5 < 2^-14.
+// Rounding to the nearest integer can then only differ when a half-integer lies within
+// 2^-14 of t; if any of the lane's 8 values is that close, all 8 take the exact
+// quotient (rare).  Away from half-integers round-half-even equals round-half-away, and
+// round-half-even of |t| < 2^22 is the integer in the low bits of fl(t + 1.5 * 2^23):
+// its low byte is the code's two's-complement byte (|t| < 127.5, so no clamp is
+// reached).  A scale outside [1e-37, 1e37] takes the exact path for every value.
 __device__ __forceinline__ void codes(const float (&v)[8], float amax, float d, uint32_t (&packed)[2]) {
+    (void)amax;
     packed[0] = packed[1] = 0u;
     if (d == 0.0f) return;  // x / d undefined: the block is stored as zero
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
     const float r = __frcp_rn(d);
-    const bool fast = d >= 1.0e-37f && d <= 1.0e37f;
+    uint32_t u[8];
+    float worst = 0.0f;  // largest |t - round(t)| of the lane
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        int q;
         const float t = __fmul_rn(v[i], r);
-        if (fast && fabsf(t - floorf(t) - 0.5f) > 3.0517578125e-05f) {  // 2^-15 from a tie
-            q = __float2int_rn(t);
-            q = q < -127 ? -127 : (q > 127 ? 127 : q);
-        } else {
-            q = code_exact(v[i], d);
-        }
-        packed[i >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (i & 3));
+        const float s = __fadd_rn(t, kRound);
+        u[i] = __float_as_uint(s);
+        worst = fmaxf(worst, fabsf(__fsub_rn(t, __fsub_rn(s, kRound))));
     }
+    if (d >= 1.0e-37f && d <= 1.0e37f && worst < 0.5f - 6.103515625e-05f) {  // 2^-14 from a tie
+        packed[0] = __byte_perm(__byte_perm(u[0], u[1], 0x0040), __byte_perm(u[2], u[3], 0x0040), 0x5410);
+        packed[1] = __byte_perm(__byte_perm(u[4], u[5], 0x0040), __byte_perm(u[6], u[7], 0x0040), 0x5410);
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        packed[i >> 2] |= (static_cast<uint32_t>(code_exact(v[i], d)) & 0xffu) << (8 * (i & 3));
 }
 
 }  // namespace q8m

@@ -48,7 +48,7 @@ constexpr int kWarps = 8;            // warps per CTA of the grouped (MoE) kerne
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPartials = 4096;   // unit sums held in shared memory per batch
 constexpr int kMaxLog2Seg = 6;       // at most 64 K-segments per row
-constexpr int kPrefetchSteps = 2;    // steps prefetched into L2 before the dependency wait
+constexpr int kPrefetchSteps = 1;    // steps prefetched into L2 before the dependency wait
 constexpr int kStepBytes = 1024;
 
 constexpr int log2_warps(int nw) { return nw == 16 ? 4 : 3; }
