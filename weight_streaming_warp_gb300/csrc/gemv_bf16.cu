@@ -79,19 +79,21 @@ struct Bf16 {
     template <bool XS>
     __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
         if constexpr (XS) {
+            // 32-bit indices: x is staged only for K <= 25600 (kMaxSmemSteps)
             float4 *xs = reinterpret_cast<float4 *>(xsm);
-            const int64_t nchunks = static_cast<int64_t>(nsteps) * 32;
+            const int K = static_cast<int>(a.K);
+            const int nchunks = nsteps * 32;
             const bool xvec = (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
-            for (int64_t q = threadIdx.x; q < 4 * nchunks; q += blockDim.x) {
+            for (int q = static_cast<int>(threadIdx.x); q < 4 * nchunks; q += static_cast<int>(blockDim.x)) {
                 // quad q = elements 4q .. 4q+3 = plane (q & 3) of chunk q >> 2
-                const int64_t e0 = 4 * q;
+                const int e0 = 4 * q;
                 float4 v;
-                if (xvec && e0 + 4 <= a.K) {
+                if (xvec && e0 + 4 <= K) {
                     v = __ldg(reinterpret_cast<const float4 *>(a.x) + q);
                 } else {
                     float t[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) t[i] = (e0 + i < a.K) ? __ldg(a.x + e0 + i) : 0.0f;
+                    for (int i = 0; i < 4; ++i) t[i] = (e0 + i < K) ? __ldg(a.x + e0 + i) : 0.0f;
                     v = make_float4(t[0], t[1], t[2], t[3]);
                 }
                 xs[(q & 3) * nchunks + (q >> 2)] = v;

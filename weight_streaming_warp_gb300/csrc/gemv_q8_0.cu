@@ -82,15 +82,18 @@ struct Q8 {
     // Shared memory: xq as two planes of 16-byte halves [2][nsteps * 32], then xd.
     template <bool XS>
     __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
+        // 32-bit indices: K <= 2^24 (checked on the host)
         uint4 *xs = reinterpret_cast<uint4 *>(xsm);
-        const int64_t nslots = static_cast<int64_t>(nsteps) * 32;
+        const int nslots = nsteps * 32;
         uint16_t *xs_d = reinterpret_cast<uint16_t *>(xs + 2 * nslots);
-        const int64_t nblk = a.K / 32;
+        const int K = static_cast<int>(a.K);
+        const int nblk = K / 32;
+        const int bd = static_cast<int>(blockDim.x);
         const bool xvec = (reinterpret_cast<uintptr_t>(a.xq) & 15) == 0;
-        for (int64_t h = threadIdx.x; h < 2 * nslots; h += blockDim.x) {
+        for (int h = static_cast<int>(threadIdx.x); h < 2 * nslots; h += bd) {
             // half h = bytes 16h .. 16h+15 = plane (h & 1) of block h >> 1
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (16 * h < a.K) {
+            if (16 * h < K) {
                 if (xvec) {
                     v = __ldg(reinterpret_cast<const uint4 *>(a.xq) + h);
                 } else {
@@ -102,7 +105,7 @@ struct Q8 {
             }
             xs[(h & 1) * nslots + (h >> 1)] = v;
         }
-        for (int64_t b = threadIdx.x; b < nslots; b += blockDim.x) xs_d[b] = b < nblk ? a.xd[b] : 0;
+        for (int b = static_cast<int>(threadIdx.x); b < nslots; b += bd) xs_d[b] = b < nblk ? a.xd[b] : 0;
     }
     template <bool XS>
     __device__ __forceinline__ static XVal load_x(const Args &, const unsigned char *xsm, int step, int lane,
