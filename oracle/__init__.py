@@ -40,6 +40,9 @@ def lib():
         L.orc_dequant_q8_0_kv.restype = None
         L.orc_attn_decode.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, i64, i64, ctypes.c_double, p]
         L.orc_attn_decode.restype = None
+        L.orc_attn_prefill.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, i64, i64, i64,
+                                       ctypes.c_double, p]
+        L.orc_attn_prefill.restype = i32
         _lib = L
     return _lib
 
@@ -171,3 +174,29 @@ def attn_decode(q, k_bits, v_bits, scale, layout="per_head"):
     lib().orc_attn_decode(_ptr(q), _ptr(k), _ptr(v), depth, heads, group, hd, ps, hs, ps, hs,
                           float(scale), _ptr(out))
     return out
+
+
+def attn_prefill(q_bits, k_bits, v_bits, scale, layout="per_head"):
+    """q uint16 (binary16 bits) [heads][group][nq][head_dim]; k, v uint16 laid out
+    [heads][depth][head_dim] ("per_head") or [depth][heads][head_dim] ("position_major")
+    -> out fp64 [heads][group][nq][head_dim].  Query i sits at position depth - nq + i
+    and sees positions 0 .. depth - nq + i."""
+    q = _c(q_bits, np.uint16)
+    k = _c(k_bits, np.uint16)
+    v = _c(v_bits, np.uint16)
+    heads, group, nq, hd = q.shape
+    if layout == "per_head":
+        depth = k.shape[1]
+        ps, hs = hd, depth * hd
+    elif layout == "position_major":
+        depth = k.shape[0]
+        ps, hs = heads * hd, hd
+    else:
+        raise ValueError(layout)
+    out = np.zeros((heads, group, nq, hd), np.float64)
+    rc = lib().orc_attn_prefill(_ptr(q), _ptr(k), _ptr(v), depth, heads, group, nq, hd, ps, hs, ps, hs,
+                                float(scale), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
+

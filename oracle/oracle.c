@@ -344,3 +344,65 @@ void orc_attn_decode(const float *q, const uint16_t *k, const uint16_t *v, int64
     }
     free(s);
 }
+
+/* ---------------------------------------------------------------------------
+ * attn_prefill  ([P1] Overview: the prefill flash-attention pass, pp512, reads the
+ * binary16 K and V of one layer; the stride discussion gives the two layouts)
+ *
+ * A batch of nq query positions at the end of a cache of `depth` positions: query i
+ * (0 <= i < nq) sits at position depth - nq + i and attends to positions
+ * 0 .. depth - nq + i (causal; the batch's own keys are the last nq positions).
+ *   s_p          = scale * sum_d q[h][g][i][d] * K(h, p)[d]
+ *   out[h][g][i] = sum_p exp(s_p - m) V(h, p) / sum_p exp(s_p - m),  m = max_p s_p
+ * in fp64 over the visible positions.  q is binary16 [heads][group][nq][head_dim];
+ * K(h, p) is the row of head_dim binary16 values at k + h * k_head_stride +
+ * p * k_pos_stride (elements), V likewise; out is fp64 [heads][group][nq][head_dim].
+ * Returns 0, or -1 for arguments outside the contract (nq < 1 or nq > depth).
+ * ------------------------------------------------------------------------- */
+int orc_attn_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t depth,
+                     int64_t heads, int64_t group, int64_t nq, int64_t head_dim,
+                     int64_t k_pos_stride, int64_t k_head_stride, int64_t v_pos_stride,
+                     int64_t v_head_stride, double scale, double *out)
+{
+    if (nq < 1 || nq > depth || heads < 0 || group < 1 || head_dim < 1)
+        return -1;
+    double *s = (double *)malloc((size_t)depth * sizeof(double));
+    double *qd = (double *)malloc((size_t)head_dim * sizeof(double));
+    for (int64_t h = 0; h < heads; ++h) {
+        for (int64_t g = 0; g < group; ++g) {
+            for (int64_t i = 0; i < nq; ++i) {
+                const uint16_t *qv = q + ((h * group + g) * nq + i) * head_dim;
+                double *o = out + ((h * group + g) * nq + i) * head_dim;
+                const int64_t visible = depth - nq + i + 1; /* positions 0 .. depth - nq + i */
+                for (int64_t d = 0; d < head_dim; ++d)
+                    qd[d] = (double)orc_f16_to_f32(qv[d]);
+                double m = -HUGE_VAL;
+                for (int64_t p = 0; p < visible; ++p) {
+                    const uint16_t *kr = k + h * k_head_stride + p * k_pos_stride;
+                    double dot = 0.0;
+                    for (int64_t d = 0; d < head_dim; ++d)
+                        dot += qd[d] * (double)orc_f16_to_f32(kr[d]);
+                    s[p] = scale * dot;
+                    if (s[p] > m)
+                        m = s[p];
+                }
+                double den = 0.0;
+                for (int64_t d = 0; d < head_dim; ++d)
+                    o[d] = 0.0;
+                for (int64_t p = 0; p < visible; ++p) {
+                    const uint16_t *vr = v + h * v_head_stride + p * v_pos_stride;
+                    double w = exp(s[p] - m);
+                    den += w;
+                    for (int64_t d = 0; d < head_dim; ++d)
+                        o[d] += w * (double)orc_f16_to_f32(vr[d]);
+                }
+                for (int64_t d = 0; d < head_dim; ++d)
+                    o[d] /= den;
+            }
+        }
+    }
+    free(qd);
+    free(s);
+    return 0;
+}
+
