@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define WSW_ABI_VERSION 5
+#define WSW_ABI_VERSION 6
 
 typedef enum wsw_status {
     WSW_OK = 0,
@@ -342,6 +342,37 @@ int wsw_attn_decode_f16(const float *q, const uint16_t *k, const uint16_t *v, in
                         int64_t k_head_stride, int64_t v_pos_stride, int64_t v_head_stride,
                         float scale, float *out, void *ws, size_t ws_bytes, void *stream,
                         const wsw_launch_opts *opts);
+
+/*
+ * wsw_attn_prefill_f16 -- causal prefill attention over a binary16 KV cache on the tensor
+ * cores: the flash-attention pass of prompt processing that reads the dequantized
+ * scratch ([P1] Overview: pp512 at depth 32768 and 65536 over the binary16 K and V; the
+ * stride discussion: the cache keeps one head's rows head_dim * n_head_kv elements
+ * apart, the scratch back to back).
+ *
+ * A batch of nq queries at the end of a cache of `depth` positions: query i of query
+ * head (h, g) sits at position depth - nq + i and attends to positions
+ * 0 .. depth - nq + i:
+ *   s_p          = scale * sum_d q[h][g][i][d] * K(h, p)[d]
+ *   out[h][g][i] = sum_p exp(s_p - m) V(h, p) / sum_p exp(s_p - m),  m = max_p s_p
+ * K(h, p) is the row of head_dim binary16 values at k + h * k_head_stride +
+ * p * k_pos_stride (elements); V likewise (the per-head scratch of
+ * wsw_dequant_q8_0_kv: strides (head_dim, depth * head_dim); the position-major cache:
+ * (heads * head_dim, head_dim)).  Products of binary16 values (q, K, V and the
+ * probabilities P, rounded to binary16) accumulate in fp32; P's rounding bounds an
+ * output element's error by about 2^-11 * (sum_p w_p |V(h, p)| / sum_p w_p + |out|).
+ *
+ *   q      binary16 [heads][group][nq][head_dim], 16-byte aligned.
+ *   k, v   binary16, 16-byte aligned; strides multiples of 8 elements.
+ *   out    fp32 [heads][group][nq][head_dim], 16-byte aligned; must not overlap inputs.
+ *   1 <= nq <= depth < 2^31;  head_dim == 128;  heads * group <= 65535
+ *   (WSW_ERR_UNSUPPORTED / WSW_ERR_INVALID_ARG otherwise).  heads == 0 does nothing.
+ * One launch; a bounded wait that gives up leaves NaN in the rows of its query tile.
+ */
+int wsw_attn_prefill_f16(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t depth,
+                         int64_t heads, int64_t group, int64_t nq, int64_t head_dim, int64_t k_pos_stride,
+                         int64_t k_head_stride, int64_t v_pos_stride, int64_t v_head_stride, float scale,
+                         float *out, void *stream, const wsw_launch_opts *opts);
 
 /*
  * wsw_gemm_bf16 -- small-batch prefill product on the tensor cores ([P2] Results:

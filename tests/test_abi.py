@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert wsw.abi_version() == 5
+    assert wsw.abi_version() == 6
     assert wsw.status_string(0) == "WSW_OK"
     assert wsw.status_string(1) == "WSW_ERR_INVALID_ARG"
     assert wsw.status_string(2) == "WSW_ERR_MISALIGNED"
@@ -134,6 +134,19 @@ def test_other_calls_reject_on_host(lib):
     assert att(kps=132) == MISALIGNED
     assert att(k=P(4104)) == MISALIGNED
     assert att(wsn=100) == 4  # WSW_ERR_WORKSPACE
+    pf = lib.wsw_attn_prefill_f16
+
+    def pre(depth=1024, heads=4, group=8, nq=512, hd=128, kps=128, khs=131072, vps=128, vhs=131072, q=A, k=A,
+            out=A):
+        return pf(q, k, A, depth, heads, group, nq, hd, kps, khs, vps, vhs, ctypes.c_float(0.1), out, None, None)
+    assert pre(nq=0) == INVALID
+    assert pre(depth=100, nq=512) == INVALID  # the batch is longer than the cache
+    assert pre(q=None) == INVALID
+    assert pre(hd=64) == UNSUPPORTED
+    assert pre(depth=1 << 31) == UNSUPPORTED
+    assert pre(kps=132) == MISALIGNED
+    assert pre(out=P(4100)) == MISALIGNED
+    assert pre(heads=0, q=None, k=None, out=None) == 0
     b = lib.wsw_bounded_wait_check
     assert b(2, P(4096), None) == INVALID
     assert b(0, None, None) == INVALID

@@ -20,7 +20,7 @@ __all__ = [
     "LaunchOpts", "WswError", "library_path", "load", "quantize_q8", "gemv_bf16",
     "gemv_bf16_chain", "gemv_q8_0", "quantize_gemv_q8_0", "moe_gemv_q8_0", "dequant_q8_0_kv", "gemm_bf16",
     "upload_padded", "status_string", "abi_version", "moe_workspace_bytes", "gemv_bf16_plan",
-    "bounded_wait_check", "attn_decode_f16", "attn_decode_workspace_bytes",
+    "bounded_wait_check", "attn_decode_f16", "attn_decode_workspace_bytes", "attn_prefill_f16",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -97,9 +97,11 @@ def load():
     L.wsw_attn_decode_workspace_bytes.restype = ctypes.c_size_t
     L.wsw_attn_decode_f16.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _p, _p,
                                       ctypes.c_size_t, _p, _p]
+    L.wsw_attn_prefill_f16.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32,
+                                       _p, _p, _p]
     for f in ("wsw_quantize_q8", "wsw_gemv_bf16", "wsw_gemv_bf16_chain", "wsw_gemv_q8_0", "wsw_quantize_gemv_q8_0",
               "wsw_moe_gemv_q8_0", "wsw_dequant_q8_0_kv", "wsw_gemm_bf16", "wsw_gemv_bf16_plan",
-              "wsw_bounded_wait_check", "wsw_attn_decode_f16"):
+              "wsw_bounded_wait_check", "wsw_attn_decode_f16", "wsw_attn_prefill_f16"):
         getattr(L, f).restype = ctypes.c_int
     _lib = L
     return L
@@ -340,6 +342,31 @@ def attn_decode_f16(q, k, v, scale=None, out=None, ws=None, opts=None):
                                       k.stride(1), k.stride(0), v.stride(1), v.stride(0), float(scale),
                                       y.data_ptr(), ws.data_ptr(), ws.numel(), _stream(), _opts(opts)),
            "attn_decode_f16")
+    return y
+
+
+def attn_prefill_f16(q, k, v, scale=None, out=None, opts=None):
+    """Causal prefill attention on the tensor cores.  q fp16 [heads][group][nq][head_dim]
+    (contiguous); k and v fp16 views indexed [head][position][dim] with unit stride in
+    dim and any head and position strides (multiples of 8).  Query i sits at position
+    depth - nq + i and sees positions 0 .. depth - nq + i.  scale defaults to
+    1/sqrt(head_dim).  Returns out fp32 [heads][group][nq][head_dim]."""
+    _dev(q, torch.float16, "q")
+    _dev(k, torch.float16, "k")
+    _dev(v, torch.float16, "v")
+    if q.dim() != 4 or not q.is_contiguous():
+        raise WswError("q must be a contiguous [heads][group][nq][head_dim] tensor")
+    heads, group, nq, hd = q.shape
+    for t, n in ((k, "k"), (v, "v")):
+        if t.dim() != 3 or t.shape[0] != heads or t.shape[2] != hd or t.shape[1] != k.shape[1] or t.stride(2) != 1:
+            raise WswError("%s must be a [heads][depth][head_dim] view with unit stride in head_dim" % n)
+    depth = k.shape[1]
+    if scale is None:
+        scale = 1.0 / float(hd) ** 0.5
+    y = out if out is not None else torch.empty((heads, group, nq, hd), dtype=torch.float32, device=q.device)
+    _check(load().wsw_attn_prefill_f16(q.data_ptr(), k.data_ptr(), v.data_ptr(), depth, heads, group, nq, hd,
+                                       k.stride(1), k.stride(0), v.stride(1), v.stride(0), float(scale),
+                                       y.data_ptr(), _stream(), _opts(opts)), "attn_prefill_f16")
     return y
 
 
