@@ -20,7 +20,7 @@ activation x (length 4096, N(0,1)) quantized to q8_0 in front of it, and the
 The same line also reports: the fused quantize + GEMV kernel against the HBM roofline
 (CUDA events over back-to-back launches on distinct weight copies), the GEMV alone, the
 other hot-path calls on their configured shapes ("rows": prefill GEMM, KV dequant, decode
-attention, each grouped MoE call and its quantizer), each as plain back-to-back launches,
+and prefill attention over the binary16 KV, each grouped MoE call and its quantizer), each as plain back-to-back launches,
 PDL-linked, and where one copy fits in L2 also L2-hot (one copy repeated, labelled
 "l2hot"), the end-to-end rate through the C ABI with host buffers, the CPU oracle on a
 bounded sample (all host cores, rows cut over threads, and one core), the 27B-shaped
@@ -529,6 +529,70 @@ def measure_attn_decode(torch, wsw, dev, out):
     torch.cuda.empty_cache()
 
 
+def attn_prefill_flops(depth, heads, group, nq, hd=128):
+    """Tensor-core flops of the causal prefill pass: query i sees depth - nq + i + 1
+    positions; per position 2 hd for q.K and 2 hd for P V."""
+    visible = nq * (depth - nq) + nq * (nq + 1) // 2
+    return 4 * hd * visible * heads * group
+
+
+def measure_attn_prefill(torch, wsw, dev, out, peak_tf):
+    """Causal prefill attention, 512 queries at the end of a binary16 cache of depth
+    32768 / 65536, 4 KV heads x 128, 8 query heads per KV head; 4 copies of K and V
+    rotate.  Also the page's pass as a whole: dequantize the q8_0 K and V once into the
+    per-head scratch, then the prefill attention over it (three PDL-linked launches)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    heads, group, nq = 4, 8, 512
+    for depth in (32768, 65536):
+        copies = 4
+        Ks = [torch.randn((heads, depth, 128), generator=g, device=dev).half() for _ in range(copies)]
+        Vs = [torch.randn((heads, depth, 128), generator=g, device=dev).half() for _ in range(copies)]
+        Kc = [t.permute(1, 0, 2).contiguous() for t in Ks]
+        Vc = [t.permute(1, 0, 2).contiguous() for t in Vs]
+        q = torch.randn((heads, group, nq, 128), generator=g, device=dev).half()
+        o = torch.empty((heads, group, nq, 128), dtype=torch.float32, device=dev)
+        fl = attn_prefill_flops(depth, heads, group, nq)
+        nb = 2 * depth * heads * 128 * 2 + q.numel() * 2 + o.numel() * 4
+        for layout in ("per_head", "position_major"):
+            it = [0]
+
+            def make(pdl, hot, layout=layout, it=it):
+                def fn(stream):
+                    i = 0 if hot else it[0] % copies
+                    it[0] += 1
+                    if layout == "per_head":
+                        k, v = Ks[i], Vs[i]
+                    else:
+                        k, v = Kc[i].permute(1, 0, 2), Vc[i].permute(1, 0, 2)
+                    wsw.attn_prefill_f16(q, k, v, out=o, opts={"pdl": pdl})
+                return fn
+            t, tp, th = _rates(torch, make, 8, hot=(layout == "per_head"))
+            e = _entry(nb, t, tp, th, flops=fl)
+            e["frac_of_bf16_peak_pdl"] = round(fl / tp / 1e12 / peak_tf, 4)
+            out["attn_prefill_d%d_%s" % (depth, layout)] = e
+        del Kc, Vc
+        # dequant once (K and V, q8_0 -> per-head binary16 scratch) + prefill attention
+        kq = [torch.randint(-127, 128, (depth, heads, 128), dtype=torch.int8, device=dev, generator=g)
+              for _ in range(2)]
+        kd = [torch.rand((depth, heads, 4), device=dev, generator=g).half() for _ in range(2)]
+        sk = torch.empty((heads, depth, 128), dtype=torch.float16, device=dev)
+        sv = torch.empty((heads, depth, 128), dtype=torch.float16, device=dev)
+
+        def make_pass(pdl, hot):
+            def fn(stream):
+                wsw.dequant_q8_0_kv(kq[0], kd[0], out=sk, opts={"pdl": pdl})
+                wsw.dequant_q8_0_kv(kq[1], kd[1], out=sv, opts={"pdl": pdl})
+                wsw.attn_prefill_f16(q, sk, sv, out=o, opts={"pdl": pdl})
+            return fn
+        t, tp, _ = _rates(torch, make_pass, 8, hot=False)
+        out["dequant_then_prefill_d%d" % depth] = {"us": round(t * 1e6, 2), "us_pdl": round(tp * 1e6, 2),
+                                                   "TFLOPs_pdl": round(fl / tp / 1e12, 1),
+                                                   "calls": "dequant K, dequant V, attn_prefill"}
+        del Ks, Vs, kq, kd, sk, sv
+    torch.cuda.empty_cache()
+
+
 MOE_E, MOE_H, MOE_F, MOE_TOPK = 128, 2048, 768, 8
 
 
@@ -619,6 +683,14 @@ def measure_moe(torch, wsw, dev, out):
     return steps
 
 
+def _bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def measure_rows(torch, wsw, dev):
     """The other hot-path calls on their configured shapes (graph-amortised, inputs
     rotating over copies larger than L2 where a single copy would fit).  Each is timed
@@ -628,6 +700,7 @@ def measure_rows(torch, wsw, dev):
     measure_gemm(torch, wsw, dev, out)
     measure_dequant(torch, wsw, dev, out)
     measure_attn_decode(torch, wsw, dev, out)
+    measure_attn_prefill(torch, wsw, dev, out, _bf16_peak())
     moe_steps = measure_moe(torch, wsw, dev, out)
     return out, moe_steps
 
@@ -868,6 +941,11 @@ def run_ours(args):
             key["config1_gemv_bf16"] = {"GBps_pdl": config1["GBps_pdl"], "GBps": config1["GBps"],
                                         "frac_pdl": round(config1["GBps_pdl"] / peak, 4),
                                         "GBps_l2hot": config1["GBps_l2hot"]}
+        if rows is not None:
+            key["attn_prefill_TFLOPs_pdl"] = {
+                "d%d" % d: rows["attn_prefill_d%d_per_head" % d]["TFLOPs_pdl"] for d in (32768, 65536)}
+            key["attn_prefill_frac_of_bf16_peak"] = {
+                "d%d" % d: rows["attn_prefill_d%d_per_head" % d]["frac_of_bf16_peak_pdl"] for d in (32768, 65536)}
         if moe_steps is not None:
             key["config4_moe_step_us_pdl"] = {"T%d" % T: s["us_pdl"] for T, s in moe_steps.items()}
             key["config4_moe_step_GBps_pdl"] = {"T%d" % T: s["GBps_pdl"] for T, s in moe_steps.items()}
@@ -916,6 +994,7 @@ def profile_case(argv):
         python bench.py --profile-case moe [T [gate_up|down]]
         python bench.py --profile-case quantize [n block]
         python bench.py --profile-case attn_decode [depth group]
+        python bench.py --profile-case attn_prefill [depth]
 
     Weights rotate over copies that together exceed the 129 MB L2, so every profiled
     launch streams its weights from HBM; the device holds at most a few GB.  Inputs
@@ -984,6 +1063,14 @@ def profile_case(argv):
         q = torch.randn((4, G, 128), device=dev, generator=g)
         for i in range(launches):
             wsw.attn_decode_f16(q, Kt[i % nc], Vt[i % nc])
+    elif what == "attn_prefill":
+        D = int(argv[1]) if len(argv) > 1 else 32768
+        nc = 3
+        Kt = [torch.randn((4, D, 128), device=dev, generator=g).half() for _ in range(nc)]
+        Vt = [torch.randn((4, D, 128), device=dev, generator=g).half() for _ in range(nc)]
+        q = torch.randn((4, 8, 512, 128), device=dev, generator=g).half()
+        for i in range(launches):
+            wsw.attn_prefill_f16(q, Kt[i % nc], Vt[i % nc])
     elif what == "quantize":
         n = int(argv[1]) if len(argv) > 1 else 4096
         block = int(argv[2]) if len(argv) > 2 else 32

@@ -360,11 +360,12 @@ int wsw_attn_decode_f16(const float *q, const uint16_t *k, const uint16_t *v, in
  * wsw_dequant_q8_0_kv: strides (head_dim, depth * head_dim); the position-major cache:
  * (heads * head_dim, head_dim)).  Products of binary16 values (q, K, V and the
  * probabilities P, rounded to binary16) accumulate in fp32; P's rounding bounds an
- * output element's error by about 2^-11 * (sum_p w_p |V(h, p)| / sum_p w_p + |out|).
+ * output element's error by about 2^-11 * sum_p w_p |V(h, p)| / sum_p w_p.
  *
  *   q      binary16 [heads][group][nq][head_dim], 16-byte aligned.
  *   k, v   binary16, 16-byte aligned; strides multiples of 8 elements.
  *   out    fp32 [heads][group][nq][head_dim], 16-byte aligned; must not overlap inputs.
+ *   scale  finite and > 0.
  *   1 <= nq <= depth < 2^31;  head_dim == 128;  heads * group <= 65535
  *   (WSW_ERR_UNSUPPORTED / WSW_ERR_INVALID_ARG otherwise).  heads == 0 does nothing.
  * One launch; a bounded wait that gives up leaves NaN in the rows of its query tile.

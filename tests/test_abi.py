@@ -146,6 +146,7 @@ def test_other_calls_reject_on_host(lib):
     assert pre(depth=1 << 31) == UNSUPPORTED
     assert pre(kps=132) == MISALIGNED
     assert pre(out=P(4100)) == MISALIGNED
+    assert pf(A, A, A, 1024, 4, 8, 512, 128, 128, 131072, 128, 131072, ctypes.c_float(0.0), A, None, None) == INVALID
     assert pre(heads=0, q=None, k=None, out=None) == 0
     b = lib.wsw_bounded_wait_check
     assert b(2, P(4096), None) == INVALID

@@ -22,17 +22,20 @@
 //                 B = V in its natural [position][dim] layout, an MN-major operand).
 //                 S_{j+1} is issued before P_j is waited for, so the tensor core works
 //                 on the next scores while the softmax runs.
-//  * warps 2-5    one query row per thread (its tensor-memory lane).  Per tile: read
-//                 the 128 scores, mask the positions past the row's causal limit,
-//                 update the running maximum in the log2 domain, write
-//                 P = 2^(s log2(e) scale - m) as binary16 into tensor memory and add
-//                 the rounded P to the row sum l.  The maximum is raised (and O, l
-//                 rescaled by 2^(m_old - m_new)) only when a tile's maximum exceeds the
-//                 one in use by more than 8; otherwise the stale maximum stays, P <= 2^8,
-//                 and the final O / l is the same softmax.  At the end: O / l to fp32.
-//  * Precision: Q, K, V and P are binary16 in the products, scores and O accumulate in
-//    fp32.  P's rounding to binary16 (relative 2^-11) bounds the error of an output
-//    element by about 2^-11 * (sum_p w_p |V_p| / sum_p w_p + |out|).
+//  * warps 2-9    softmax: a query row per thread (its tensor-memory lane) and one half
+//                 of each tile's 128 positions per warp; the two warps of a lane quarter
+//                 combine their tile maxima through shared memory.  Per tile: read the
+//                 64 scores, mask the positions past the row's causal limit (only in the
+//                 last tiles of a query tile), take the tile maximum in the log2 domain,
+//                 write P = 2^(s scale log2(e) - m) as binary16 into tensor memory and
+//                 add P to the row sum l (packed fp32x2 arithmetic).  The maximum m in
+//                 use is raised (and O, l rescaled by 2^(m_old - m_new)) only when a
+//                 tile's maximum exceeds it by more than 8; otherwise the stale maximum
+//                 stays, P <= 2^8, and the final O / l is the same softmax.  At the end:
+//                 O / l to fp32.
+//  * Precision: Q, K, V and P are binary16 in the products, scores, O and l accumulate
+//    in fp32 (l from the unrounded P).  P's rounding to binary16 (relative 2^-11) bounds
+//    the error of an output element by about 2^-11 * sum_p w_p |V_p| / sum_p w_p.
 //  * Every mbarrier wait is bounded (about a second); a role whose wait ran out stops,
 //    the rows of the tile are written as NaN, the producer waits (bounded) for its
 //    copies in flight, and tensor memory is still released.
@@ -53,8 +56,9 @@ constexpr int kHD = 128;        // head_dim
 constexpr int kBQ = 128;        // queries per tile (MMA M)
 constexpr int kBP = 128;        // positions per KV tile (MMA N of S, K of P V)
 constexpr int kKS = 2;          // K stages
-constexpr int kVS = 2;          // V stages
-constexpr int kThreadsA = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: softmax
+constexpr int kVS = 3;          // V stages (a V tile is used one softmax later than its K tile)
+constexpr int kSoftWarps = 8;   // two per tensor-memory lane quarter, one per half of a tile
+constexpr int kThreadsA = 64 + 32 * kSoftWarps;  // warp 0: TMA, warp 1: MMA, warps 2-9: softmax
 constexpr int kTile = kBP * kHD * 2;  // 32 KB: one K or V tile (two boxes of 64 dims)
 constexpr int kBox = kTile / 2;       // 16 KB: 128 rows x 128 bytes
 constexpr uint32_t kTmemCols = 512;
@@ -71,6 +75,10 @@ struct Smem {
     uint64_t s_full[2], s_free[2];
     uint64_t p_full[2], pv_done[2];
     uint64_t o_final;
+    uint64_t pair_max[2][4];  // the two warps of a lane quarter exchange tile maxima
+    uint64_t pair_sum[4];     // ... and their halves of the row sums
+    float red[2][2][kBQ];     // [tile parity][half][row]: partial tile maxima
+    float lsum[2][kBQ];       // [half][row]: partial row sums
     uint32_t tmem_slot;
 };
 
@@ -136,10 +144,21 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 2^x (MUFU); results below 2^-126 flush to zero, which no probability here needs
+// (the largest probability of a row is at least 2^-8).
 __device__ __forceinline__ float ex2(float x) {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
 }
 
 __global__ void __launch_bounds__(kThreadsA, 1)
@@ -167,10 +186,12 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         for (int i = 0; i < kVS; ++i) { mbar_init(&S.v_full[i], 1); mbar_init(&S.v_empty[i], 1); }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&S.s_full[i], 1);
-            mbar_init(&S.s_free[i], 4);
-            mbar_init(&S.p_full[i], 4);
+            mbar_init(&S.s_free[i], kSoftWarps);
+            mbar_init(&S.p_full[i], kSoftWarps);
             mbar_init(&S.pv_done[i], 1);
+            for (int qd = 0; qd < 4; ++qd) mbar_init(&S.pair_max[i][qd], 2);
         }
+        for (int qd = 0; qd < 4; ++qd) mbar_init(&S.pair_sum[qd], 2);
         mbar_init(&S.o_final, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -261,35 +282,48 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         }
         __syncwarp();
     } else {
-        // softmax: thread = query row r = its tensor-memory lane
+        // softmax: thread = query row r (its tensor-memory lane) and half hf of each tile
+        // (positions 64 hf .. 64 hf + 63); the two warps of a lane quarter combine their
+        // tile maxima through shared memory, so both use the same maximum for the row
         const int qd = warp & 3;
+        const int hf = (warp - 2) >> 2;
         const int r = 32 * qd + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
         const int64_t lim = base + q0 + (r < rows ? r : rows - 1);  // last visible position
-        float m = -INFINITY, l = 0.0f;
+        const float cs = a.scale_log2;
+        const uint64_t cs2 = f2_pack(cs, cs);
+        float m = -INFINITY;
+        uint64_t l2 = 0ull;  // two partial sums of the row's probabilities (fp32 pair)
         for (int j = 0; j < nkv; ++j) {
             const int sb = j & 1;
             if (!__all_sync(WSW_FULL_MASK, ok && mbar_wait(&S.s_full[sb], (j >> 1) & 1u))) { ok = false; break; }
             tc_fence_after();
-            uint32_t sv[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + kColS + 128 * sb + 32 * c, sv[c]);
+            uint32_t sv[2][32];
+            tmem_ld32(lane_base + kColS + 128 * sb + 64 * hf, sv[0]);
+            tmem_ld32(lane_base + kColS + 128 * sb + 64 * hf + 32, sv[1]);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.s_free[sb]);
-            // scores in the log2 domain, in place; masked positions -inf
-            float mt = -INFINITY;
-            const int64_t p0 = static_cast<int64_t>(j) * kBP;
-            const bool masking = j >= first_masked;
+            if (j >= first_masked) {
+                // positions past the row's causal limit read as -inf
+                const int64_t lc = lim - (static_cast<int64_t>(j) * kBP + 64 * hf);
+                const int last = lc < 0 ? -1 : (lc > 63 ? 63 : static_cast<int>(lc));
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                float v = __uint_as_float(sv[c >> 5][c & 31]) * a.scale_log2;
-                if (masking && p0 + c > lim) v = -INFINITY;
-                sv[c >> 5][c & 31] = __float_as_uint(v);
-                mt = fmaxf(mt, v);
+                for (int c = 0; c < 64; ++c)
+                    if (c > last) sv[c >> 5][c & 31] = 0xff800000u;
             }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(sv[c >> 5][c & 31]));
+            S.red[sb][hf][r] = mx;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.pair_max[sb][qd]);
+            if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.pair_max[sb][qd], (j >> 1) & 1u))) { ok = false; break; }
+            // scale > 0, so the maximum of the scaled scores is the scaled maximum
+            const float mt = fmaxf(S.red[sb][0][r], S.red[sb][1][r]) * cs;
             // raise the maximum in use only when this tile exceeds it by more than kLazy
+            // (both warps of the quarter decide alike: same inputs)
             const bool raise = mt > m + kLazy;
             if (j > 0 && __any_sync(WSW_FULL_MASK, raise)) {
                 // O must hold P_{j-1} V_{j-1} before it is rescaled
@@ -299,16 +333,24 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 }
                 tc_fence_after();
                 const float alpha = raise ? ex2(m - mt) : 1.0f;
+                const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(lane_base + kColO + 32 * c, o);
+                    tmem_ld32(lane_base + kColO + 64 * hf + 32 * c, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(lane_base + kColO + 32 * c, o);
+                    for (int i = 0; i < 32; i += 2) {
+                        uint64_t v = f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1]));
+                        asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(v) : "l"(al2));
+                        float x0, x1;
+                        f2_unpack(v, x0, x1);
+                        o[i] = __float_as_uint(x0);
+                        o[i + 1] = __float_as_uint(x1);
+                    }
+                    tmem_st32(lane_base + kColO + 64 * hf + 32 * c, o);
                 }
-                l *= alpha;
+                asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(l2) : "l"(al2));
             }
             if (raise) m = mt;
             // P_j into its tensor-memory slot, free once P_{j-2} V_{j-2} has completed
@@ -317,35 +359,41 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 break;
             }
             tc_fence_after();
+            const uint64_t nm2 = f2_pack(-m, -m);
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int e = 64 * c + 2 * i;
-                    const __half2 hp = __floats2half2_rn(ex2(__uint_as_float(sv[e >> 5][e & 31]) - m),
-                                                         ex2(__uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31]) - m));
-                    const float2 f = __half22float2(hp);
-                    l += f.x + f.y;
-                    pk[i] = *reinterpret_cast<const uint32_t *>(&hp);
-                }
-                tmem_st32(lane_base + kColP + 64 * sb + 32 * c, pk);
+            for (int i = 0; i < 32; ++i) {
+                const int e = 2 * i;
+                uint64_t t = f2_pack(__uint_as_float(sv[e >> 5][e & 31]), __uint_as_float(sv[(e + 1) >> 5][(e + 1) & 31]));
+                asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(t) : "l"(cs2), "l"(nm2));  // s log2(e) scale - m
+                float t0, t1;
+                f2_unpack(t, t0, t1);
+                const float p0 = ex2(t0), p1 = ex2(t1);
+                const __half2 hp = __floats2half2_rn(p0, p1);
+                pk[i] = *reinterpret_cast<const uint32_t *>(&hp);
+                asm("add.rn.f32x2 %0, %0, %1;" : "+l"(l2) : "l"(f2_pack(p0, p1)));
             }
+            tmem_st32(lane_base + kColP + 64 * sb + 32 * hf, pk);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.p_full[sb]);
         }
-        // epilogue: O / l
-        const bool have = __all_sync(WSW_FULL_MASK, ok && mbar_wait(&S.o_final, 0));
+        // epilogue: the row sum from both halves, then this half of O / l
+        float l0, l1;
+        f2_unpack(l2, l0, l1);
+        S.lsum[hf][r] = l0 + l1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.pair_sum[qd]);
+        const bool have = __all_sync(WSW_FULL_MASK, ok && mbar_wait(&S.pair_sum[qd], 0) && mbar_wait(&S.o_final, 0));
         tc_fence_after();
-        const float inv = 1.0f / l;
-        float *dst = a.out + ((static_cast<int64_t>(hg) * a.nq) + q0 + r) * kHD;
+        const float inv = 1.0f / (S.lsum[0][r] + S.lsum[1][r]);
+        float *dst = a.out + ((static_cast<int64_t>(hg) * a.nq) + q0 + r) * kHD + 64 * hf;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
             if (have) {
-                tmem_ld32(lane_base + kColO + 32 * c, o);
+                tmem_ld32(lane_base + kColO + 64 * hf + 32 * c, o);
                 tmem_wait_ld();
             }
             if (r < rows) {
@@ -414,6 +462,7 @@ extern "C" int wsw_attn_prefill_f16(const uint16_t *q, const uint16_t *k, const 
     int st = resolve_opts(opts, &o);
     if (st != WSW_OK) return st;
     if (heads < 0 || group < 1 || nq < 1 || depth < nq || head_dim < 1) return WSW_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !(scale < 3.0e38f)) return WSW_ERR_INVALID_ARG;  // finite and positive
     if (heads == 0) return WSW_OK;
     if (!q || !k || !v || !out) return WSW_ERR_INVALID_ARG;
     if (head_dim != kHD) return WSW_ERR_UNSUPPORTED;
