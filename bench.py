@@ -588,8 +588,23 @@ def measure_attn_prefill(torch, wsw, dev, out, peak_tf):
         t, tp, _ = _rates(torch, make_pass, 8, hot=False)
         out["dequant_then_prefill_d%d" % depth] = {"us": round(t * 1e6, 2), "us_pdl": round(tp * 1e6, 2),
                                                    "TFLOPs_pdl": round(fl / tp / 1e12, 1),
+                                                   "scratch_bytes": 2 * sk.numel() * 2,
                                                    "calls": "dequant K, dequant V, attn_prefill"}
-        del Ks, Vs, kq, kd, sk, sv
+        # the same pass with a bounded scratch: one window of K and V at a time
+        window = 4096 if depth == 32768 else 8192
+        ws = torch.empty(wsw.attn_prefill_q8_0_workspace_bytes(depth, heads, group, nq, window), dtype=torch.uint8,
+                         device=dev)
+
+        def make_win(pdl, hot):
+            def fn(stream):
+                wsw.attn_prefill_q8_0(q, kq[0], kd[0], kq[1], kd[1], window, out=o, ws=ws, opts={"pdl": pdl})
+            return fn
+        t, tp, _ = _rates(torch, make_win, 4, hot=False)
+        out["windowed_q8_0_prefill_d%d_w%d" % (depth, window)] = {
+            "us": round(t * 1e6, 2), "us_pdl": round(tp * 1e6, 2), "TFLOPs_pdl": round(fl / tp / 1e12, 1),
+            "frac_of_bf16_peak_pdl": round(fl / tp / 1e12 / peak_tf, 4), "workspace_bytes": ws.numel(),
+            "calls": "per window: dequant K, dequant V, attention with the carried softmax state"}
+        del Ks, Vs, kq, kd, sk, sv, ws
     torch.cuda.empty_cache()
 
 
@@ -946,6 +961,9 @@ def run_ours(args):
                 "d%d" % d: rows["attn_prefill_d%d_per_head" % d]["TFLOPs_pdl"] for d in (32768, 65536)}
             key["attn_prefill_frac_of_bf16_peak"] = {
                 "d%d" % d: rows["attn_prefill_d%d_per_head" % d]["frac_of_bf16_peak_pdl"] for d in (32768, 65536)}
+            key["windowed_q8_0_prefill_TFLOPs_pdl"] = {
+                "d32768_w4096": rows["windowed_q8_0_prefill_d32768_w4096"]["TFLOPs_pdl"],
+                "d65536_w8192": rows["windowed_q8_0_prefill_d65536_w8192"]["TFLOPs_pdl"]}
         if moe_steps is not None:
             key["config4_moe_step_us_pdl"] = {"T%d" % T: s["us_pdl"] for T, s in moe_steps.items()}
             key["config4_moe_step_GBps_pdl"] = {"T%d" % T: s["GBps_pdl"] for T, s in moe_steps.items()}

@@ -376,6 +376,41 @@ int wsw_attn_prefill_f16(const uint16_t *q, const uint16_t *k, const uint16_t *v
                          float *out, void *stream, const wsw_launch_opts *opts);
 
 /*
+ * wsw_attn_prefill_q8_0 -- the same causal prefill attention over a q8_0 KV cache, with a
+ * scratch of bounded size: the cache is dequantized and attended one window of
+ * positions at a time ([P1] author's reply, "A few directions ... as follow-ups":
+ * bounding the scratch with a chunked / streamed scratch that caps the peak, instead of
+ * one binary16 layer of K and V for the whole depth; the dequantization is [P1]'s
+ * dequant-once pass, wsw_dequant_q8_0_kv, applied to each window).
+ *
+ * For each window of `window` positions (the last one may be shorter): dequantize the
+ * window's K and V rows into the per-head binary16 scratch, then attend over them,
+ * carrying every query row's online-softmax state (running maximum, sum and unnormalized
+ * output) from window to window.  Three launches per window, PDL-linked with opts->pdl.
+ * The result equals wsw_dequant_q8_0_kv of K and V followed by wsw_attn_prefill_f16
+ * within that call's stated error bound (not bit for bit: the maximum the
+ * probabilities are taken against can differ between the two).
+ *
+ *   q        binary16 [heads][group][nq][head_dim], 16-byte aligned.
+ *   kq, vq   int8 [depth][heads][head_dim];  kd, vd binary16 [depth][heads][head_dim/32]
+ *            (the cache layout wsw_dequant_q8_0_kv reads).
+ *   window   positions per window: a multiple of 128, at least 128.
+ *   ws       device workspace of ws_bytes >= wsw_attn_prefill_q8_0_workspace_bytes(...)
+ *            bytes, 256-byte aligned, overwritten (WSW_ERR_WORKSPACE otherwise): the K and
+ *            V scratch of one window (2 * heads * min(window, depth) * head_dim * 2 bytes)
+ *            and, with more than one window, the state (heads * group * nq * 528 bytes).
+ *            Two calls in flight at once need two workspaces.
+ *   out      as wsw_attn_prefill_f16.
+ * Other limits as wsw_attn_prefill_f16.
+ */
+size_t wsw_attn_prefill_q8_0_workspace_bytes(int64_t depth, int64_t heads, int64_t group, int64_t nq,
+                                             int64_t window);
+int wsw_attn_prefill_q8_0(const uint16_t *q, const int8_t *kq, const uint16_t *kd, const int8_t *vq,
+                          const uint16_t *vd, int64_t depth, int64_t heads, int64_t group, int64_t nq,
+                          int64_t head_dim, float scale, int64_t window, void *ws, size_t ws_bytes, float *out,
+                          void *stream, const wsw_launch_opts *opts);
+
+/*
  * wsw_gemm_bf16 -- small-batch prefill product on the tensor cores ([P2] Results:
  * small-batch prefill streams the whole weight matrix for a short run of output
  * rows; the weight's row stride may carry one extra 128-byte line).

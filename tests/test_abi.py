@@ -148,6 +148,21 @@ def test_other_calls_reject_on_host(lib):
     assert pre(out=P(4100)) == MISALIGNED
     assert pf(A, A, A, 1024, 4, 8, 512, 128, 128, 131072, 128, 131072, ctypes.c_float(0.0), A, None, None) == INVALID
     assert pre(heads=0, q=None, k=None, out=None) == 0
+    wb = lib.wsw_attn_prefill_q8_0_workspace_bytes
+    wb.restype = ctypes.c_size_t
+    one = 4 * 4096 * 128 * 2  # one window of K (or V) as binary16
+    assert wb(32768, 4, 8, 512, 4096) == 2 * one + 4 * 8 * 512 * 132 * 4
+    assert wb(4096, 4, 8, 512, 4096) == 2 * one  # a single window carries no state
+    assert wb(4096, 4, 8, 512, 100) == 0 and wb(0, 4, 8, 512, 128) == 0
+    p8 = lib.wsw_attn_prefill_q8_0
+
+    def pq(window=256, ws=A, wsn=1 << 30, kq=A):
+        return p8(A, kq, A, A, A, 1024, 4, 8, 512, 128, ctypes.c_float(0.1), window, ws, ctypes.c_size_t(wsn), A,
+                  None, None)
+    assert pq(window=200) == INVALID
+    assert pq(kq=None) == INVALID
+    assert pq(wsn=1000) == 4  # WSW_ERR_WORKSPACE
+    assert pq(ws=P(4112)) == 4  # not 256-byte aligned
     b = lib.wsw_bounded_wait_check
     assert b(2, P(4096), None) == INVALID
     assert b(0, None, None) == INVALID

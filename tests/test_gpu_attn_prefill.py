@@ -13,7 +13,13 @@ batch that fills the cache (its first query sees one position), a single query, 
 of the page's layouts, large scores (the running maximum is raised mid-row), the
 dequant-then-attend pipeline, and the configured depths 32768 and 65536 with 4 KV heads,
 8 query heads each and 512 queries, checked on sampled queries (each one is the oracle
-for a single query at the end of its visible prefix)."""
+for a single query at the end of its visible prefix).
+
+The windowed q8_0 pass (dequantize and attend one window of positions at a time, the
+online-softmax state carried between windows) is checked the same way against the
+oracle's attention over the oracle's dequantized cache: short last windows, windows past
+the causal limit of early query tiles, one window, large scores, and the configured
+depths with windows of 4096 and 8192 positions."""
 import math
 
 import numpy as np
@@ -148,3 +154,67 @@ def test_config_depths_sampled_queries(orc, depth, layout):
                                        np.ascontiguousarray(vb[h:h + 1, :vis]), scale)[0, 0, 0]
                 mag = _magnitude_row(qf[h, g, i], kb[h, :vis], vb[h, :vis], scale)
                 _check_row(got[h, g, i], ref, mag, "d%d %s h%d g%d i%d" % (depth, layout, h, g, i))
+
+
+# ----------------------------------------------------------- windowed q8_0 pass --
+
+def _q8_cache(orc, seed, heads, depth):
+    """A q8_0 K or V cache [depth][heads][128] (+ scales) quantized by the oracle from
+    N(0, 1) binary16 values, and its dequantized per-head binary16 form (the oracle's)."""
+    x = syn.normal(seed, "q8kv%d_%d" % (heads, depth), (depth * heads, 128), dtype=torch.float16).float().numpy()
+    q, d = orc.quantize_q8(x, 32)
+    q, d = q.reshape(depth, heads, 128), d.reshape(depth, heads, 4)
+    return q, d, orc.dequant_q8_0_kv(q, d)
+
+
+def _run_windowed(wsw, orc, seed, heads, group, nq, depth, window, qsigma=1.0):
+    kq, kd, kb = _q8_cache(orc, seed, heads, depth)
+    vq, vd, vb = _q8_cache(orc, seed + 1, heads, depth)
+    q = syn.normal(seed, "wq%d_%d_%d" % (heads, group, nq), (heads, group, nq, 128), qsigma, torch.float16)
+    scale = 1.0 / math.sqrt(128)
+    got = wsw.attn_prefill_q8_0(q.cuda(), torch.from_numpy(kq).cuda(), u16_to_torch(kd, torch.float16).cuda(),
+                                torch.from_numpy(vq).cuda(), u16_to_torch(vd, torch.float16).cuda(), window, scale)
+    torch.cuda.synchronize()
+    return q, kb, vb, got.cpu().double().numpy(), scale
+
+
+@pytest.mark.parametrize("heads,group,nq,depth,window", [
+    (2, 2, 300, 1000, 256),   # four windows, the last one short
+    (1, 2, 600, 700, 128),    # windows past the limit of early query tiles
+    (2, 1, 100, 900, 1024),   # one window: no carried state
+    (1, 1, 1, 777, 384)])     # a single query
+def test_windowed_q8_0_every_row(orc, heads, group, nq, depth, window):
+    """Dequantize-and-attend one window at a time against the oracle's attention over the
+    oracle's dequantized cache."""
+    wsw = need_gpu()
+    q, kb, vb, got, scale = _run_windowed(wsw, orc, 7, heads, group, nq, depth, window)
+    _check_all(orc, q, torch.from_numpy(kb.view(np.int16)).view(torch.float16),
+               torch.from_numpy(vb.view(np.int16)).view(torch.float16), got, scale, "windowed w%d" % window)
+
+
+def test_windowed_q8_0_large_scores(orc):
+    """Peaked scores: the carried maximum is raised in later windows."""
+    wsw = need_gpu()
+    q, kb, vb, got, scale = _run_windowed(wsw, orc, 8, 1, 2, 200, 1500, 256, qsigma=6.0)
+    _check_all(orc, q, torch.from_numpy(kb.view(np.int16)).view(torch.float16),
+               torch.from_numpy(vb.view(np.int16)).view(torch.float16), got, scale, "windowed large scores")
+
+
+@pytest.mark.parametrize("depth,window", [(32768, 4096), (65536, 8192)])
+def test_windowed_q8_0_config_depths_sampled_queries(orc, depth, window):
+    """The configured cache (4 KV heads, 8 query heads each, 512 queries) through a scratch
+    of one window, checked on sampled queries of every query head."""
+    wsw = need_gpu()
+    heads, group, nq = 4, 8, 512
+    q, kb, vb, got, scale = _run_windowed(wsw, orc, 9, heads, group, nq, depth, window)
+    qb = f16_bits(q)
+    qf = qb.view(np.float16).astype(np.float64)
+    for h in range(heads):
+        for g in range(group):
+            for i in (0, 127, 128, 384, 511):
+                vis = depth - nq + i + 1
+                ref = orc.attn_prefill(np.ascontiguousarray(qb[h:h + 1, g:g + 1, i:i + 1]),
+                                       np.ascontiguousarray(kb[h:h + 1, :vis]),
+                                       np.ascontiguousarray(vb[h:h + 1, :vis]), scale)[0, 0, 0]
+                mag = _magnitude_row(qf[h, g, i], kb[h, :vis], vb[h, :vis], scale)
+                _check_row(got[h, g, i], ref, mag, "windowed d%d w%d h%d g%d i%d" % (depth, window, h, g, i))

@@ -21,6 +21,7 @@ __all__ = [
     "gemv_bf16_chain", "gemv_q8_0", "quantize_gemv_q8_0", "moe_gemv_q8_0", "dequant_q8_0_kv", "gemm_bf16",
     "upload_padded", "status_string", "abi_version", "moe_workspace_bytes", "gemv_bf16_plan",
     "bounded_wait_check", "attn_decode_f16", "attn_decode_workspace_bytes", "attn_prefill_f16",
+    "attn_prefill_q8_0", "attn_prefill_q8_0_workspace_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -99,6 +100,11 @@ def load():
                                       ctypes.c_size_t, _p, _p]
     L.wsw_attn_prefill_f16.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32,
                                        _p, _p, _p]
+    L.wsw_attn_prefill_q8_0_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i64]
+    L.wsw_attn_prefill_q8_0_workspace_bytes.restype = ctypes.c_size_t
+    L.wsw_attn_prefill_q8_0.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _f32, _i64, _p,
+                                        ctypes.c_size_t, _p, _p, _p]
+    L.wsw_attn_prefill_q8_0.restype = ctypes.c_int
     for f in ("wsw_quantize_q8", "wsw_gemv_bf16", "wsw_gemv_bf16_chain", "wsw_gemv_q8_0", "wsw_quantize_gemv_q8_0",
               "wsw_moe_gemv_q8_0", "wsw_dequant_q8_0_kv", "wsw_gemm_bf16", "wsw_gemv_bf16_plan",
               "wsw_bounded_wait_check", "wsw_attn_decode_f16", "wsw_attn_prefill_f16"):
@@ -367,6 +373,39 @@ def attn_prefill_f16(q, k, v, scale=None, out=None, opts=None):
     _check(load().wsw_attn_prefill_f16(q.data_ptr(), k.data_ptr(), v.data_ptr(), depth, heads, group, nq, hd,
                                        k.stride(1), k.stride(0), v.stride(1), v.stride(0), float(scale),
                                        y.data_ptr(), _stream(), _opts(opts)), "attn_prefill_f16")
+    return y
+
+
+def attn_prefill_q8_0_workspace_bytes(depth, heads, group, nq, window) -> int:
+    return int(load().wsw_attn_prefill_q8_0_workspace_bytes(depth, heads, group, nq, window))
+
+
+def attn_prefill_q8_0(q, kq, kd, vq, vd, window, scale=None, out=None, ws=None, opts=None):
+    """Causal prefill attention over a q8_0 KV cache, dequantized and attended one window
+    of `window` positions at a time (a multiple of 128), so the binary16 scratch holds one
+    window of K and V.  q fp16 [heads][group][nq][head_dim]; kq, vq int8
+    [depth][heads][head_dim]; kd, vd fp16 [depth][heads][head_dim/32].  ws: a uint8 device
+    tensor of at least attn_prefill_q8_0_workspace_bytes(...) bytes, allocated if None.
+    Returns out fp32 [heads][group][nq][head_dim]."""
+    _dev(q, torch.float16, "q")
+    for t, n, dt in ((kq, "kq", torch.int8), (vq, "vq", torch.int8), (kd, "kd", torch.float16),
+                     (vd, "vd", torch.float16)):
+        _dev(t, dt, n)
+        if not t.is_contiguous():
+            raise WswError("%s must be contiguous" % n)
+    if q.dim() != 4 or not q.is_contiguous():
+        raise WswError("q must be a contiguous [heads][group][nq][head_dim] tensor")
+    heads, group, nq, hd = q.shape
+    depth = kq.shape[0]
+    if scale is None:
+        scale = 1.0 / float(hd) ** 0.5
+    y = out if out is not None else torch.empty((heads, group, nq, hd), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = torch.empty(max(attn_prefill_q8_0_workspace_bytes(depth, heads, group, nq, window), 1),
+                         dtype=torch.uint8, device=q.device)
+    _check(load().wsw_attn_prefill_q8_0(q.data_ptr(), kq.data_ptr(), kd.data_ptr(), vq.data_ptr(), vd.data_ptr(),
+                                        depth, heads, group, nq, hd, float(scale), int(window), ws.data_ptr(),
+                                        ws.numel(), y.data_ptr(), _stream(), _opts(opts)), "attn_prefill_q8_0")
     return y
 
 

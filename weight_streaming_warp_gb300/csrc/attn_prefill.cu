@@ -82,11 +82,21 @@ struct Smem {
     uint32_t tmem_slot;
 };
 
+// One launch attends over the cache positions [pos0, pos0 + npos) of a cache of `depth`
+// positions; K and V hold just those rows (a window of the cache, or all of it).  Between
+// the windows of one batch the online-softmax state of every query row travels through
+// `state`: fp32 [heads * group * nq][kStateStride] = (m, l, -, -, O[128]), O unnormalized
+// and m the log2-domain maximum that P and O are relative to.
+constexpr int kStateStride = 132;
+
 struct AttnArgs {
     int64_t depth, nq;
+    int64_t pos0, npos;  // the window of this launch
     int heads, group, qtiles;
-    float scale_log2;  // scale * log2(e)
+    int first, last;     // first window (no incoming state), last window (write out)
+    float scale_log2;    // scale * log2(e)
     float *out;
+    float *state;        // NULL when first && last
 };
 
 // MN-major operand (V as B of P V): 128-byte swizzle, 64-element atoms along N
@@ -175,10 +185,18 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     const int h = hg / a.group;
     const int64_t q0 = static_cast<int64_t>(t) * kBQ;
     const int64_t rows = a.nq - q0 < kBQ ? a.nq - q0 : kBQ;
-    const int64_t base = a.depth - a.nq;                  // position of query 0
-    const int64_t lim_last = base + q0 + rows - 1;         // last position any row sees
-    const int nkv = static_cast<int>(lim_last / kBP) + 1;  // KV tiles of this CTA
-    const int first_masked = static_cast<int>((base + q0) / kBP);  // first tile row 0 may not fully see
+    const int64_t base = a.depth - a.nq;           // position of query 0
+    const int64_t lim0 = base + q0;                 // last position row 0 sees
+    const int64_t lim_last = base + q0 + rows - 1;  // last position any row sees
+    // KV tiles of this window that some row sees, and the first one that row 0 may not
+    // see whole (past its causal limit, or past the window's last row)
+    const int64_t wtiles = (a.npos + kBP - 1) / kBP;
+    int64_t nkv64 = lim_last < a.pos0 ? 0 : (lim_last - a.pos0) / kBP + 1;
+    if (nkv64 > wtiles) nkv64 = wtiles;
+    const int nkv = static_cast<int>(nkv64);
+    int64_t fm = lim0 + 1 - a.pos0 < 0 ? 0 : (lim0 + 1 - a.pos0) / kBP;
+    if (fm > a.npos / kBP) fm = a.npos / kBP;
+    const int first_masked = static_cast<int>(fm);
 
     if (threadIdx.x == 0) {
         mbar_init(&S.q_full, 1);
@@ -207,7 +225,26 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     const uint32_t tmem = S.tmem_slot;
     bool ok = true;
 
-    if (warp == 0) {
+    if (nkv == 0) {
+        // no position of this window is visible to the tile: only the last window has
+        // work, the output from the incoming state
+        if (warp >= 2 && a.last) {
+            pdl_wait();  // the state is written by the window before, maybe still running
+            const int qd = warp & 3, hf = (warp - 2) >> 2;
+            const int r = 32 * qd + lane;
+            if (r < rows) {
+                const int64_t row = static_cast<int64_t>(hg) * a.nq + q0 + r;
+                const float *st = a.state + row * kStateStride;
+                const float inv = 1.0f / st[1];
+                float *dst = a.out + row * kHD + 64 * hf;
+#pragma unroll
+                for (int i = 0; i < 64; i += 4) {
+                    const float4 o = *reinterpret_cast<const float4 *>(st + 4 + 64 * hf + i);
+                    *reinterpret_cast<float4 *>(dst + i) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+                }
+            }
+        }
+    } else if (warp == 0) {
         if (lane == 0) {
             uint64_t pol_q, pol_kv;
             asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_q));
@@ -274,7 +311,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 const uint64_t dv = sw128_mn_desc(saddr(S.v[vs]), kBox);
 #pragma unroll
                 for (int kk = 0; kk < kBP / 16; ++kk)  // 16 positions per MMA: 8 P columns, 2 KB of V
-                    mma_ts(tmem + kColO, tmem + kColP + 64 * pb + 8 * kk, dv + 128 * kk, id_pv, (j | kk) != 0);
+                    mma_ts(tmem + kColO, tmem + kColP + 64 * pb + 8 * kk, dv + 128 * kk, id_pv,
+                           (j | kk) != 0 || !a.first);
                 mma_commit(&S.v_empty[vs]);
                 mma_commit(&S.pv_done[pb]);
             }
@@ -290,10 +328,18 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         const int r = 32 * qd + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * qd) << 16);
         const int64_t lim = base + q0 + (r < rows ? r : rows - 1);  // last visible position
+        // last visible row of the window for this thread's row
+        const int64_t lim_w = (lim - a.pos0 < a.npos - 1 ? lim - a.pos0 : a.npos - 1);
+        const int64_t srow = static_cast<int64_t>(hg) * a.nq + q0 + (r < rows ? r : rows - 1);
         const float cs = a.scale_log2;
         const uint64_t cs2 = f2_pack(cs, cs);
         float m = -INFINITY;
         uint64_t l2 = 0ull;  // two partial sums of the row's probabilities (fp32 pair)
+        if (!a.first) {  // the state of the earlier windows: m, and l in half 0's sum
+            pdl_wait();  // written by the window before, maybe still running
+            m = a.state[srow * kStateStride];
+            if (hf == 0) l2 = f2_pack(a.state[srow * kStateStride + 1], 0.0f);
+        }
         for (int j = 0; j < nkv; ++j) {
             const int sb = j & 1;
             if (!__all_sync(WSW_FULL_MASK, ok && mbar_wait(&S.s_full[sb], (j >> 1) & 1u))) { ok = false; break; }
@@ -306,8 +352,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.s_free[sb]);
             if (j >= first_masked) {
-                // positions past the row's causal limit read as -inf
-                const int64_t lc = lim - (static_cast<int64_t>(j) * kBP + 64 * hf);
+                // positions past the row's causal limit or the window's end read as -inf
+                const int64_t lc = lim_w - (static_cast<int64_t>(j) * kBP + 64 * hf);
                 const int last = lc < 0 ? -1 : (lc > 63 ? 63 : static_cast<int>(lc));
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
@@ -325,7 +371,20 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             // raise the maximum in use only when this tile exceeds it by more than kLazy
             // (both warps of the quarter decide alike: same inputs)
             const bool raise = mt > m + kLazy;
-            if (j > 0 && __any_sync(WSW_FULL_MASK, raise)) {
+            if (j == 0 && !a.first) {
+                // O of the earlier windows into tensor memory, rescaled to the maximum in use
+                const float alpha = raise ? ex2(m - mt) : 1.0f;
+                const float *so = a.state + srow * kStateStride + 4 + 64 * hf;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t o[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(so[32 * c + i] * alpha);
+                    tmem_st32(lane_base + kColO + 64 * hf + 32 * c, o);
+                }
+                const uint64_t al2 = f2_pack(alpha, alpha);
+                asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(l2) : "l"(al2));
+            } else if (j > 0 && __any_sync(WSW_FULL_MASK, raise)) {
                 // O must hold P_{j-1} V_{j-1} before it is rescaled
                 if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1u))) {
                     ok = false;
@@ -387,10 +446,38 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         if (lane == 0) mbar_arrive(&S.pair_sum[qd]);
         const bool have = __all_sync(WSW_FULL_MASK, ok && mbar_wait(&S.pair_sum[qd], 0) && mbar_wait(&S.o_final, 0));
         tc_fence_after();
-        const float inv = 1.0f / (S.lsum[0][r] + S.lsum[1][r]);
+        const float lrow = S.lsum[0][r] + S.lsum[1][r];
+        if (!a.last) {
+            // hand the state on: m, l and this half of the unnormalized O
+            float *st = a.state + srow * kStateStride;
+            if (r < rows && hf == 0) {
+                st[0] = have ? m : __int_as_float(0x7fc00000);
+                st[1] = have ? lrow : __int_as_float(0x7fc00000);
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t o[32];
+                if (have) {
+                    tmem_ld32(lane_base + kColO + 64 * hf + 32 * c, o);
+                    tmem_wait_ld();
+                }
+                if (r < rows) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        float4 w;
+                        w.x = have ? __uint_as_float(o[i]) : __int_as_float(0x7fc00000);
+                        w.y = have ? __uint_as_float(o[i + 1]) : __int_as_float(0x7fc00000);
+                        w.z = have ? __uint_as_float(o[i + 2]) : __int_as_float(0x7fc00000);
+                        w.w = have ? __uint_as_float(o[i + 3]) : __int_as_float(0x7fc00000);
+                        *reinterpret_cast<float4 *>(st + 4 + 64 * hf + 32 * c + i) = w;
+                    }
+                }
+            }
+        }
+        const float inv = 1.0f / lrow;
         float *dst = a.out + ((static_cast<int64_t>(hg) * a.nq) + q0 + r) * kHD + 64 * hf;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 2 && a.last; ++c) {
             uint32_t o[32];
             if (have) {
                 tmem_ld32(lane_base + kColO + 64 * hf + 32 * c, o);
@@ -449,6 +536,66 @@ bool make_map3(CUtensorMap *map, const void *base, int64_t d1, int64_t d2, int64
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One launch over the window [pos0, pos0 + npos) of the cache (K and V hold its rows);
+// arguments already validated.
+int attn_launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t depth, int64_t heads,
+                int64_t group, int64_t nq, int64_t kps, int64_t khs, int64_t vps, int64_t vhs, int64_t pos0,
+                int64_t npos, bool first, bool last, float *state, float scale, float *out, cudaStream_t s,
+                bool pdl, const DeviceInfo &di) {
+    const size_t smem = sizeof(Smem) + 1024;
+    if (smem > static_cast<size_t>(di.max_smem_optin)) return WSW_ERR_UNSUPPORTED;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(attn_prefill_kernel), static_cast<int>(smem));
+    if (e != cudaSuccess) return WSW_ERR_CUDA;
+    CUtensorMap tmQ, tmK, tmV;
+    const int64_t hs_k = heads > 1 ? khs : kps * npos;
+    const int64_t hs_v = heads > 1 ? vhs : vps * npos;
+    if (!make_map3(&tmQ, q, nq, heads * group, kHD * 2, nq * kHD * 2) ||
+        !make_map3(&tmK, k, npos, heads, kps * 2, hs_k * 2) || !make_map3(&tmV, v, npos, heads, vps * 2, hs_v * 2))
+        return WSW_ERR_CUDA;
+    AttnArgs a;
+    a.depth = depth;
+    a.nq = nq;
+    a.pos0 = pos0;
+    a.npos = npos;
+    a.heads = static_cast<int>(heads);
+    a.group = static_cast<int>(group);
+    a.qtiles = static_cast<int>((nq + kBQ - 1) / kBQ);
+    a.first = first ? 1 : 0;
+    a.last = last ? 1 : 0;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.out = out;
+    a.state = state;
+    const unsigned grid = static_cast<unsigned>(a.qtiles * heads * group);
+    e = launch(attn_prefill_kernel, dim3(grid), dim3(kThreadsA), smem, s, pdl, tmQ, tmK, tmV, a);
+    return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
+}
+
+// Checks shared by the two entry points (q, out, the shape and the scale).
+int check_common(const uint16_t *q, float *out, int64_t depth, int64_t heads, int64_t group, int64_t nq,
+                 int64_t head_dim, float scale) {
+    if (heads < 0 || group < 1 || nq < 1 || depth < nq || head_dim < 1) return WSW_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !(scale < 3.0e38f)) return WSW_ERR_INVALID_ARG;  // finite and positive
+    if (heads == 0) return WSW_OK;
+    if (!q || !out) return WSW_ERR_INVALID_ARG;
+    if (head_dim != kHD) return WSW_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15)) return WSW_ERR_MISALIGNED;
+    if (depth >= (int64_t(1) << 31) || heads * group > 65535 || (nq + kBQ - 1) / kBQ * heads * group > 0x7fffffffLL)
+        return WSW_ERR_UNSUPPORTED;
+    return WSW_OK;
+}
+
+size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+// Workspace of the windowed q8_0 pass: binary16 scratch for one window of K and of V,
+// then (with more than one window) the carried state.
+size_t q8_ws_bytes(int64_t depth, int64_t heads, int64_t group, int64_t nq, int64_t window, int64_t *nwin) {
+    const int64_t w = window < depth ? window : depth;
+    *nwin = (depth + window - 1) / window;
+    size_t n = 2 * align256(static_cast<size_t>(heads) * w * kHD * 2);
+    if (*nwin > 1) n += align256(static_cast<size_t>(heads) * group * nq * kStateStride * 4);
+    return n;
+}
+
 }  // namespace
 }  // namespace wsw
 
@@ -461,46 +608,67 @@ extern "C" int wsw_attn_prefill_f16(const uint16_t *q, const uint16_t *k, const 
     Opts o;
     int st = resolve_opts(opts, &o);
     if (st != WSW_OK) return st;
-    if (heads < 0 || group < 1 || nq < 1 || depth < nq || head_dim < 1) return WSW_ERR_INVALID_ARG;
-    if (!(scale > 0.0f) || !(scale < 3.0e38f)) return WSW_ERR_INVALID_ARG;  // finite and positive
-    if (heads == 0) return WSW_OK;
-    if (!q || !k || !v || !out) return WSW_ERR_INVALID_ARG;
-    if (head_dim != kHD) return WSW_ERR_UNSUPPORTED;
+    st = check_common(q, out, depth, heads, group, nq, head_dim, scale);
+    if (st != WSW_OK || heads == 0) return st;
+    if (!k || !v) return WSW_ERR_INVALID_ARG;
     if (k_pos_stride < 1 || k_head_stride < 0 || v_pos_stride < 1 || v_head_stride < 0) return WSW_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(k) & 15) ||
-        (reinterpret_cast<uintptr_t>(v) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) || (k_pos_stride % 8) ||
+    if ((reinterpret_cast<uintptr_t>(k) & 15) || (reinterpret_cast<uintptr_t>(v) & 15) || (k_pos_stride % 8) ||
         (k_head_stride % 8) || (v_pos_stride % 8) || (v_head_stride % 8))
         return WSW_ERR_MISALIGNED;
-    if (depth >= (int64_t(1) << 31) || heads * group > 65535 || (nq + kBQ - 1) / kBQ * heads * group > 0x7fffffffLL)
-        return WSW_ERR_UNSUPPORTED;
-    if (k_head_stride == 0 && heads > 1) return WSW_ERR_INVALID_ARG;
-    if (v_head_stride == 0 && heads > 1) return WSW_ERR_INVALID_ARG;
+    if ((k_head_stride == 0 || v_head_stride == 0) && heads > 1) return WSW_ERR_INVALID_ARG;
     DeviceInfo di;
     if (!device_info(&di, &st)) return st;
+    return attn_launch(q, k, v, depth, heads, group, nq, k_pos_stride, k_head_stride, v_pos_stride, v_head_stride, 0,
+                       depth, true, true, nullptr, scale, out, static_cast<cudaStream_t>(stream), o.pdl, di);
+}
 
-    const size_t smem = sizeof(Smem) + 1024;
-    if (smem > static_cast<size_t>(di.max_smem_optin)) return WSW_ERR_UNSUPPORTED;
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(attn_prefill_kernel), static_cast<int>(smem));
-    if (e != cudaSuccess) return WSW_ERR_CUDA;
+extern "C" size_t wsw_attn_prefill_q8_0_workspace_bytes(int64_t depth, int64_t heads, int64_t group, int64_t nq,
+                                                        int64_t window) {
+    using namespace wsw;
+    if (depth < 1 || heads < 1 || group < 1 || nq < 1 || window < kBP || window % kBP != 0) return 0;
+    int64_t nwin;
+    return q8_ws_bytes(depth, heads, group, nq, window, &nwin);
+}
 
-    CUtensorMap tmQ, tmK, tmV;
-    const int64_t hs_k = heads > 1 ? k_head_stride : k_pos_stride * depth;
-    const int64_t hs_v = heads > 1 ? v_head_stride : v_pos_stride * depth;
-    if (!make_map3(&tmQ, q, nq, heads * group, kHD * 2, nq * kHD * 2) ||
-        !make_map3(&tmK, k, depth, heads, k_pos_stride * 2, hs_k * 2) ||
-        !make_map3(&tmV, v, depth, heads, v_pos_stride * 2, hs_v * 2))
-        return WSW_ERR_CUDA;
-
-    AttnArgs a;
-    a.depth = depth;
-    a.nq = nq;
-    a.heads = static_cast<int>(heads);
-    a.group = static_cast<int>(group);
-    a.qtiles = static_cast<int>((nq + kBQ - 1) / kBQ);
-    a.scale_log2 = scale * 1.4426950408889634f;
-    a.out = out;
-    const unsigned grid = static_cast<unsigned>(a.qtiles * heads * group);
-    e = launch(attn_prefill_kernel, dim3(grid), dim3(kThreadsA), smem, static_cast<cudaStream_t>(stream), o.pdl,
-               tmQ, tmK, tmV, a);
-    return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
+extern "C" int wsw_attn_prefill_q8_0(const uint16_t *q, const int8_t *kq, const uint16_t *kd, const int8_t *vq,
+                                     const uint16_t *vd, int64_t depth, int64_t heads, int64_t group, int64_t nq,
+                                     int64_t head_dim, float scale, int64_t window, void *ws, size_t ws_bytes,
+                                     float *out, void *stream, const wsw_launch_opts *opts) {
+    using namespace wsw;
+    Opts o;
+    int st = resolve_opts(opts, &o);
+    if (st != WSW_OK) return st;
+    st = check_common(q, out, depth, heads, group, nq, head_dim, scale);
+    if (st != WSW_OK || heads == 0) return st;
+    if (!kq || !kd || !vq || !vd) return WSW_ERR_INVALID_ARG;
+    if (window < kBP || window % kBP != 0) return WSW_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(kd) & 1) || (reinterpret_cast<uintptr_t>(vd) & 1)) return WSW_ERR_MISALIGNED;
+    int64_t nwin;
+    const size_t need = q8_ws_bytes(depth, heads, group, nq, window, &nwin);
+    if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return WSW_ERR_WORKSPACE;
+    DeviceInfo di;
+    if (!device_info(&di, &st)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t w = window < depth ? window : depth;
+    uint16_t *sk = static_cast<uint16_t *>(ws);
+    uint16_t *sv = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + align256(static_cast<size_t>(heads) * w * kHD * 2));
+    float *state = nwin > 1 ? reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                                        2 * align256(static_cast<size_t>(heads) * w * kHD * 2))
+                            : nullptr;
+    wsw_launch_opts dq = {0, 0, o.pdl ? 1 : 0, 0, 0};
+    for (int64_t i = 0; i < nwin; ++i) {
+        const int64_t pos0 = i * window;
+        const int64_t npos = depth - pos0 < window ? depth - pos0 : window;
+        // this window of K and V, dequantized into the per-head scratch [heads][npos][128]
+        st = wsw_dequant_q8_0_kv(kq + pos0 * heads * kHD, kd + pos0 * heads * (kHD / 32), npos, heads, kHD, sk, stream,
+                                 &dq);
+        if (st != WSW_OK) return st;
+        st = wsw_dequant_q8_0_kv(vq + pos0 * heads * kHD, vd + pos0 * heads * (kHD / 32), npos, heads, kHD, sv, stream,
+                                 &dq);
+        if (st != WSW_OK) return st;
+        st = attn_launch(q, sk, sv, depth, heads, group, nq, kHD, npos * kHD, kHD, npos * kHD, pos0, npos, i == 0,
+                         i == nwin - 1, state, scale, out, s, o.pdl, di);
+        if (st != WSW_OK) return st;
+    }
+    return WSW_OK;
 }
