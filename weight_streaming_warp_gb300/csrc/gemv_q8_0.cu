@@ -231,11 +231,16 @@ struct Q8G : Q8 {
     }
     // per-token bytes of the staged activation: Q8's two 16-byte planes and the scales
     __device__ __forceinline__ static int64_t token_bytes(int nsteps) { return static_cast<int64_t>(nsteps) * 1088; }
+    // routed row of virtual row v: 32-bit division (v < R * Mo <= 16 * 2^24)
+    __device__ __forceinline__ static uint32_t routed_row(const Args &a, int64_t v) {
+        return static_cast<uint32_t>(v) / static_cast<uint32_t>(a.Mo);
+    }
     __device__ __forceinline__ static int64_t expert_row(const Args &a, int64_t v, bool &valid) {
-        const int64_t m = v / a.Mo;
+        const uint32_t m = routed_row(a, v);
         const int e = ids_smem()[m];
         valid = e >= 0;
-        return static_cast<int64_t>(valid ? e : 0) * a.Mo + (v - m * a.Mo);
+        const uint32_t o = static_cast<uint32_t>(v) - m * static_cast<uint32_t>(a.Mo);
+        return static_cast<int64_t>(valid ? e : 0) * a.Mo + o;
     }
     __device__ __forceinline__ static const char *row_ptr(const Args &a, int64_t v) {
         bool valid;
@@ -259,22 +264,25 @@ struct Q8G : Q8 {
             ids_smem()[threadIdx.x] = ok ? e : -1;
             if (!ok && blockIdx.x == 0 && a.err) atomicOr(a.err, 1);
         }
-        const int64_t nslots = static_cast<int64_t>(nsteps) * 32;
-        const int64_t tb = token_bytes(nsteps);
-        const int64_t nblk = a.K / 32;
+        // 32-bit indices: R <= 16 and K <= 2^24
+        const int nslots = nsteps * 32;
+        const int tb = nsteps * 1088;
+        const int K = static_cast<int>(a.K);
+        const int nblk = K / 32;
+        const int bd = static_cast<int>(blockDim.x);
         const bool xvec = (reinterpret_cast<uintptr_t>(a.xq) & 15) == 0;
-        const int64_t nh = 2 * nslots;  // 16-byte halves of one routed row (padded past K)
-        const int64_t total = a.R * nh;
-        for (int64_t i0 = threadIdx.x; i0 < total; i0 += 4 * static_cast<int64_t>(blockDim.x)) {
+        const int nh = 2 * nslots;  // 16-byte halves of one routed row (padded past K)
+        const int total = static_cast<int>(a.R) * nh;
+        for (int i0 = static_cast<int>(threadIdx.x); i0 < total; i0 += 4 * bd) {
             uint4 v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int64_t i = i0 + u * static_cast<int64_t>(blockDim.x);
+                const int i = i0 + u * bd;
                 v[u] = make_uint4(0u, 0u, 0u, 0u);
                 if (i < total) {
-                    const int64_t m = i / nh, h = i - m * nh;
-                    const int8_t *row = a.xq + m * a.K;
-                    if (16 * h < a.K) {
+                    const int m = i / nh, h = i - m * nh;
+                    const int8_t *row = a.xq + static_cast<int64_t>(m) * K;
+                    if (16 * h < K) {
                         if (xvec) {
                             v[u] = __ldg(reinterpret_cast<const uint4 *>(row) + h);
                         } else {
@@ -288,31 +296,31 @@ struct Q8G : Q8 {
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int64_t i = i0 + u * static_cast<int64_t>(blockDim.x);
+                const int i = i0 + u * bd;
                 if (i < total) {
-                    const int64_t m = i / nh, h = i - m * nh;
+                    const int m = i / nh, h = i - m * nh;
                     // half h = bytes 16h .. 16h+15 = plane (h & 1) of block h >> 1
                     reinterpret_cast<uint4 *>(xsm + m * tb)[(h & 1) * nslots + (h >> 1)] = v[u];
                 }
             }
         }
-        const int64_t dtotal = a.R * nslots;
-        for (int64_t i0 = threadIdx.x; i0 < dtotal; i0 += 4 * static_cast<int64_t>(blockDim.x)) {
+        const int dtotal = static_cast<int>(a.R) * nslots;
+        for (int i0 = static_cast<int>(threadIdx.x); i0 < dtotal; i0 += 4 * bd) {
             uint16_t dv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int64_t i = i0 + u * static_cast<int64_t>(blockDim.x);
+                const int i = i0 + u * bd;
                 dv[u] = 0;
                 if (i < dtotal) {
-                    const int64_t m = i / nslots, b = i - m * nslots;
+                    const int m = i / nslots, b = i - m * nslots;
                     if (b < nblk) dv[u] = a.xd[m * nblk + b];
                 }
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int64_t i = i0 + u * static_cast<int64_t>(blockDim.x);
+                const int i = i0 + u * bd;
                 if (i < dtotal) {
-                    const int64_t m = i / nslots, b = i - m * nslots;
+                    const int m = i / nslots, b = i - m * nslots;
                     reinterpret_cast<uint16_t *>(xsm + m * tb + 32 * nslots)[b] = dv[u];
                 }
             }
@@ -321,10 +329,10 @@ struct Q8G : Q8 {
     template <bool XS>
     __device__ __forceinline__ static XVal load_x(const Args &a, const unsigned char *xsm, int step, int lane,
                                                   int nsteps, int64_t row) {
-        return Q8::load_x<XS>(a, xsm + (row / a.Mo) * token_bytes(nsteps), step, lane, nsteps);
+        return Q8::load_x<XS>(a, xsm + routed_row(a, row) * token_bytes(nsteps), step, lane, nsteps);
     }
     __device__ __forceinline__ static void store(const Args &a, int64_t v, float s) {
-        if (ids_smem()[v / a.Mo] >= 0) a.y[v] = s;
+        if (ids_smem()[routed_row(a, v)] >= 0) a.y[v] = s;
     }
 };
 
