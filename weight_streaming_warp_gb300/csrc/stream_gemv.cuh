@@ -114,13 +114,23 @@ __device__ __forceinline__ void prefetch_next_link(const NextLink &nx, int wid, 
     }
 }
 
-template <class F, int R, int LB, bool XS, bool SPLIT>
-__global__ void __launch_bounds__(F::kWarps * 32, 16 / F::kWarps) stream_gemv_kernel(const typename F::Args a) {
+// The dependency protocol of one mat-vec launch: wait for the previous kernel in the
+// stream (programmatic dependent launch), then let the next one be scheduled.
+struct PdlWait {
+    __device__ __forceinline__ void before() const { pdl_wait(); }
+    __device__ __forceinline__ void after() const { pdl_launch_dependents(); }
+};
+
+// One mat-vec by one CTA, the body of stream_gemv_kernel.  `wait.before()` is where the
+// CTA waits for the data an earlier kernel (or link) writes; every thread of the CTA
+// calls it exactly once, after its first weight loads are in flight (before them for
+// kWaitFirst formats).  `wait.after()` follows the staging of x.
+template <class F, int R, int LB, bool XS, bool SPLIT, class Wait>
+__device__ __forceinline__ void matvec_body(const typename F::Args &a, unsigned char *smem, const Wait &wait) {
     constexpr int U = 4 / R;  // steps per register batch
     constexpr int NW = F::kWarps;
     constexpr int LW = log2_warps(NW);
     static_assert(NW == 8 || NW == 16, "8 or 16 warps per CTA");
-    extern __shared__ __align__(16) unsigned char smem[];
     float *part = reinterpret_cast<float *>(smem);
     unsigned char *xsm = smem + (SPLIT ? kMaxPartials * sizeof(float) : 0);
 
@@ -207,10 +217,10 @@ __global__ void __launch_bounds__(F::kWarps * 32, 16 / F::kWarps) stream_gemv_ke
         // on their way into L2.
         if constexpr (F::kWaitFirst) {
             if (!started) {
-                pdl_wait();
+                wait.before();
                 F::template stage_x<XS>(a, xsm, nsteps);
                 __syncthreads();
-                pdl_launch_dependents();
+                wait.after();
                 started = true;
             }
         }
@@ -232,10 +242,10 @@ __global__ void __launch_bounds__(F::kWarps * 32, 16 / F::kWarps) stream_gemv_ke
             }
         }
         if (!started) {
-            pdl_wait();
+            wait.before();
             F::template stage_x<XS>(a, xsm, nsteps);
             __syncthreads();
-            pdl_launch_dependents();
+            wait.after();
             started = true;
         }
 
@@ -306,10 +316,16 @@ __global__ void __launch_bounds__(F::kWarps * 32, 16 / F::kWarps) stream_gemv_ke
     }
     if (!started) {
         // A CTA without rows takes part in the dependency protocol all the same.
-        pdl_wait();
-        pdl_launch_dependents();
+        wait.before();
+        wait.after();
     }
     if constexpr (HasNextLink<F>::value) prefetch_next_link<NW>(a.nx, wid, lane);
+}
+
+template <class F, int R, int LB, bool XS, bool SPLIT>
+__global__ void __launch_bounds__(F::kWarps * 32, 16 / F::kWarps) stream_gemv_kernel(const typename F::Args a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    matvec_body<F, R, LB, XS, SPLIT>(a, smem, PdlWait{});
 }
 
 // K-segments per row (log2) for an M x (nsteps warp steps) matrix on `sm_count` SMs and
