@@ -232,24 +232,9 @@ __global__ void __launch_bounds__(kT, 2) moe_cc_kernel(const MoeArgs a) {
     struct Buf { uint32_t w[kRows][8]; uint32_t d[kRows]; };
     Buf bufA[kU], bufB[kU];
 
-    // The activation rows of a unit into L1 when its first weight loads are issued, so
-    // that the multiply finds them there (every step of the unit reads them).
-    const int xlines = static_cast<int>((a.K + 127) / 128), dlines = static_cast<int>((a.K / 16 + 127) / 128);
-    auto prefetch_unit_x = [&](const Unit &t) {
-        const int per = xlines + dlines;
-        for (int i = lane; i < t.n * per; i += 32) {
-            const int tt = i / per, li = i - tt * per;
-            const int64_t m = list[t.tok0 + tt];
-            const char *p = li < xlines ? reinterpret_cast<const char *>(a.xq + m * a.K) + 128 * li
-                                        : reinterpret_cast<const char *>(a.xd + m * nblk) + 128 * (li - xlines);
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-        }
-    };
-
     Unit iu;
     iu.ui = 0;
     locate(0, iu);
-    prefetch_unit_x(iu);
     int iq = 0, ist = 0;
     auto issue = [&](Buf(&buf)[kU]) {
 #pragma unroll
@@ -270,12 +255,8 @@ __global__ void __launch_bounds__(kT, 2) moe_cc_kernel(const MoeArgs a) {
                 }
                 if (++ist == nsteps) {
                     ist = 0;
-                    if (--iu.np > 0) {
-                        iu.o += kRows;
-                    } else if (++iq < nq) {
-                        locate(iq, iu);
-                        prefetch_unit_x(iu);
-                    }
+                    if (--iu.np > 0) iu.o += kRows;
+                    else if (++iq < nq) locate(iq, iu);
                 }
             }
         }
