@@ -306,6 +306,9 @@ int wsw_moe_gemv_q8_0_noalloc(const int8_t *Wq, const uint16_t *Wd, int64_t E, i
  *   q     int8 [depth][heads][head_dim];  head_dim % 32 == 0.
  *   d     binary16 [depth][heads][head_dim/32].
  *   out   binary16 [heads][depth][head_dim]; must not overlap the inputs.
+ * Returns WSW_ERR_INVALID_ARG for negative sizes, head_dim % 32 != 0, depth > 2^32,
+ * heads or head_dim > 65536, or more than 2^45 values; WSW_ERR_MISALIGNED for an odd d
+ * or out address.  Any size of zero is a no-op.
  */
 int wsw_dequant_q8_0_kv(const int8_t *q, const uint16_t *d, int64_t depth, int64_t heads,
                         int64_t head_dim, uint16_t *out, void *stream,

@@ -61,6 +61,30 @@ def test_ragged(orc, M, K, N):
     _check(orc, W, X, Y, np.arange(M), "%dx%dx%d" % (M, K, N))
 
 
+@pytest.mark.parametrize("M,K,N", [(2560, 8192, 300), (10240, 64, 512)])
+def test_wide_batches(orc, M, K, N):
+    """Batches of more than 256 rows (two batch tiles): split over a cluster (2560 x 8192,
+    ragged N) and more weight tiles than SMs (10240 x 64).  Whole tiles and the ragged
+    last batch rows against the fp64 oracle; every output against an fp32 product
+    within the same bound."""
+    wsw = need_gpu()
+    W = syn.normal(3, "W2a%d_%d" % (M, K), (M, K), 0.02, torch.bfloat16)
+    X = syn.normal(3, "X2a%d_%d" % (N, K), (N, K), 1.0, torch.bfloat16)
+    Wd, Xd = W.cuda(), X.cuda()
+    Y = wsw.gemm_bf16(Wd, Xd)
+    tiles = [0, 1, M // 128 - 1]
+    rows = np.unique(np.concatenate([np.arange(t * 128, t * 128 + 128, 2) for t in tiles] + [[M - 1]]))
+    _check(orc, W, X, Y, rows, "%dx%dx%d" % (M, K, N))
+    tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        ref = Xd.float() @ Wd.float().T
+        mag = Xd.float().abs() @ Wd.float().abs().T
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+    assert ((Y - ref).abs() <= TOL_BF16 * mag + 1e-30).all()
+
+
 def test_rejects_misaligned():
     wsw = need_gpu()
     W = torch.zeros((16, 72), dtype=torch.bfloat16, device="cuda")

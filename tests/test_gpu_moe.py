@@ -238,3 +238,46 @@ def test_misaligned_weights_are_bit_identical(orc):
     for m in range(R):
         yd = wsw.gemv_q8_0(Wqd[ids[m]], Wdd[ids[m]], xqd[m], xdd[m])
         assert torch.equal(yd.view(torch.int32), y[m].view(torch.int32)), m
+
+
+@pytest.mark.parametrize("Mo,K,R,En", [(64, 256, 17, 3), (99, 800, 100, 5), (256, 768, 256, 40), (1536, 2048, 128, 128)])
+def test_bucketed_form_rows_equal_dense(orc, Mo, K, R, En):
+    """17 to 256 routed rows (the bucketed CUDA-core form): many repeated experts, an odd
+    Mo, a bad id; rows equal the dense mat-vec on their expert bit for bit for every
+    launch option, and activations off a 16-byte boundary give the same bits."""
+    wsw = need_gpu()
+    g = np.random.default_rng(Mo + K + R)
+    Wq = g.integers(-127, 128, size=(En, Mo, K)).astype(np.int8)
+    Wd = g.integers(0x0800, 0x1c00, size=(En, Mo, K // 32)).astype(np.uint16)
+    xq = g.integers(-127, 128, size=(R, K)).astype(np.int8)
+    xd = g.integers(0x0800, 0x1c00, size=(R, K // 32)).astype(np.uint16)
+    ids = g.integers(0, En, size=R).astype(np.int32)
+    ids[R // 2] = -3  # out of range
+    Wqd, Wdd = torch.from_numpy(Wq).cuda(), u16_to_torch(Wd, torch.float16).cuda()
+    xqd, xdd = torch.from_numpy(xq).cuda(), u16_to_torch(xd, torch.float16).cuda()
+    idd = torch.from_numpy(ids).cuda()
+    ref = None
+    for opts in (None, {"rows_per_warp": 1}, {"rows_per_warp": 4, "load_bytes": 8}, {"pdl": 1, "ctas_per_sm": 1}):
+        y = torch.full((R, Mo), 7.0, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        wsw.moe_gemv_q8_0(Wqd, Wdd, xqd, xdd, idd, out=y, err_flag=err, opts=opts)
+        if ref is None:
+            ref = y.clone()
+        assert torch.equal(y.view(torch.int32), ref.view(torch.int32)), opts
+        assert err.item() == 1
+    assert (ref[R // 2] == 7.0).all()
+    raw = torch.zeros(xq.size + 8, dtype=torch.int8, device="cuda")
+    xmis = raw[8:].view(R, K)
+    xmis.copy_(xqd)
+    ym = torch.full((R, Mo), 7.0, device="cuda")
+    wsw.moe_gemv_q8_0(Wqd, Wdd, xmis, xdd, idd, out=ym)
+    assert torch.equal(ym.view(torch.int32), ref.view(torch.int32))
+    for m in range(R):
+        if m == R // 2:
+            continue
+        if m % 7 == 0 or m < 4:
+            yd = wsw.gemv_q8_0(Wqd[ids[m]], Wdd[ids[m]], xqd[m], xdd[m])
+            assert torch.equal(yd.view(torch.int32), ref[m].view(torch.int32)), m
+        if m % 31 == 0:
+            check_tol(ref[m].cpu().numpy(), orc.gemv_q8_0(Wq[ids[m]], Wd[ids[m]], xq[m], xd[m]),
+                      mag_q8(Wq[ids[m]], Wd[ids[m]], xq[m], xd[m]), TOL_Q8, "row %d" % m)

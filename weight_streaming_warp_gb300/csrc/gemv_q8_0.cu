@@ -254,16 +254,19 @@ struct Q8G : Q8 {
         else Q8::zero(b);
     }
     __device__ __forceinline__ static void prefetch_x(const Args &) {}
-    // All R activations in one pass over (routed row, 16-byte piece) pairs, four loads in
-    // flight per thread before their stores, in Q8's layout per routed row.
-    template <bool XS>
-    __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
+    // The routing ids, before the first weight load.
+    __device__ __forceinline__ static void stage_route(const Args &a) {
         if (threadIdx.x < a.R) {
             const int e = a.ids[threadIdx.x];
             const bool ok = e >= 0 && e < a.E;
             ids_smem()[threadIdx.x] = ok ? e : -1;
             if (!ok && blockIdx.x == 0 && a.err) atomicOr(a.err, 1);
         }
+    }
+    // All R activations in one pass over (routed row, 16-byte piece) pairs, four loads in
+    // flight per thread before their stores, in Q8's layout per routed row.
+    template <bool XS>
+    __device__ __forceinline__ static void stage_x(const Args &a, unsigned char *xsm, int nsteps) {
         // 32-bit indices: R <= 16 and K <= 2^24
         const int nslots = nsteps * 32;
         const int tb = nsteps * 1088;

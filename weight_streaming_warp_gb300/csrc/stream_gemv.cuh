@@ -30,8 +30,9 @@
 // and load / row_ptr / row_bytes / prefetch_x / stage_x / load_x / accumulate /
 // lane_total / store.  load_x also receives the first row of the group (a format whose
 // activation differs by row picks it from there).  kWaitFirst: the weight addresses
-// depend on data written by earlier kernels, so the dependency wait and stage_x come
-// before the first weight load.  A format whose Args has a NextLink `nx` also requests
+// depend on data written by earlier kernels, so the dependency wait and the format's
+// stage_route (which stages that data) come before the first weight load, and stage_x
+// follows it.  A format whose Args has a NextLink `nx` also requests
 // into L2, once its warps are done, what the next mat-vec of a chain reads first.
 // A step is 1 KB of a row in both formats.
 #pragma once
@@ -215,16 +216,17 @@ __device__ __forceinline__ void matvec_body(const typename F::Args &a, unsigned 
         // both register batches are then in flight before the dependency wait, i.e.
         // while the previous kernel in the stream drains, and the steps after them are
         // on their way into L2.
-        if constexpr (F::kWaitFirst) {
-            if (!started) {
+        // A kWaitFirst format waits first and stages what its weight addresses depend on
+        // (stage_route); its weight loads are then in flight while it stages x.
+        if (!started) {
+            if constexpr (F::kWaitFirst) {
                 wait.before();
-                F::template stage_x<XS>(a, xsm, nsteps);
+                F::stage_route(a);
                 __syncthreads();
-                wait.after();
-                started = true;
+            } else {
+                F::prefetch_x(a);
             }
         }
-        if (!started) F::prefetch_x(a);
         issue(bufA);
         issue(bufB);
         if (!started) {
@@ -242,7 +244,7 @@ __device__ __forceinline__ void matvec_body(const typename F::Args &a, unsigned 
             }
         }
         if (!started) {
-            wait.before();
+            if constexpr (!F::kWaitFirst) wait.before();
             F::template stage_x<XS>(a, xsm, nsteps);
             __syncthreads();
             wait.after();
