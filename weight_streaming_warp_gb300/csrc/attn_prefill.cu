@@ -13,8 +13,12 @@
 //
 // Design (GB300, one CTA per (KV head, query head, tile of 128 queries)):
 //  * warp 0       TMA: the query tile once (128 x 128 binary16, two 128-byte-swizzled
-//                 boxes of 64 dims), then K and V tiles of 128 positions into rings of
-//                 kKS and kVS stages.
+//                 boxes of 64 dims), then K tiles of 128 positions into a ring of kKS
+//                 stages.
+//  * warp 10      TMA: V tiles of 128 positions into a ring of kVS stages.  K and V have
+//                 producers of their own, so that neither ring waits behind the other:
+//                 a tile takes about 1.5 us to land, and K is needed a softmax earlier
+//                 than V.
 //  * warp 1       owns tensor memory (512 columns: O [0, 128), two score buffers S of
 //                 128 columns, two P buffers of 64 columns) and one thread issues the
 //                 MMAs: S_j = Q K_j^T (A = Q, B = K, both K-major in shared memory) and
@@ -55,10 +59,12 @@ using namespace tc;
 constexpr int kHD = 128;        // head_dim
 constexpr int kBQ = 128;        // queries per tile (MMA M)
 constexpr int kBP = 128;        // positions per KV tile (MMA N of S, K of P V)
-constexpr int kKS = 2;          // K stages
-constexpr int kVS = 3;          // V stages (a V tile is used one softmax later than its K tile)
+constexpr int kKS = 3;          // K stages (a K tile is needed one softmax before its V tile)
+constexpr int kVS = 2;          // V stages
 constexpr int kSoftWarps = 8;   // two per tensor-memory lane quarter, one per half of a tile
-constexpr int kThreadsA = 64 + 32 * kSoftWarps;  // warp 0: TMA, warp 1: MMA, warps 2-9: softmax
+constexpr int kVWarp = 2 + kSoftWarps;  // the V producer
+// warp 0: Q and K TMA, warp 1: MMA, warps 2-9: softmax, warp 10: V TMA
+constexpr int kThreadsA = 32 * (kVWarp + 1);
 constexpr int kTile = kBP * kHD * 2;  // 32 KB: one K or V tile (two boxes of 64 dims)
 constexpr int kBox = kTile / 2;       // 16 KB: 128 rows x 128 bytes
 constexpr uint32_t kTmemCols = 512;
@@ -228,7 +234,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     if (nkv == 0) {
         // no position of this window is visible to the tile: only the last window has
         // work, the output from the incoming state
-        if (warp >= 2 && a.last) {
+        if (warp >= 2 && warp < kVWarp && a.last) {
             pdl_wait();  // the state is written by the window before, maybe still running
             const int qd = warp & 3, hf = (warp - 2) >> 2;
             const int r = 32 * qd + lane;
@@ -251,32 +257,45 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_kv));
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
-            pdl_wait();  // Q, K and V may be written by earlier kernels in the stream
+            pdl_wait();  // Q and K may be written by earlier kernels in the stream
             mbar_expect_tx(&S.q_full, kTile);
             for (int b = 0; b < 2; ++b)
                 tma_load_3d(S.q + b * kBox, &tmQ, 64 * b, static_cast<int>(q0), hg, &S.q_full, pol_q);
-            int issued_k = 0, issued_v = 0;
+            int issued = 0;
             for (int j = 0; j < nkv && ok; ++j) {
-                const int ks = j % kKS, vs = j % kVS;
+                const int ks = j % kKS;
                 if (j >= kKS && !mbar_wait(&S.k_empty[ks], ((j / kKS) - 1) & 1u)) { ok = false; break; }
                 mbar_expect_tx(&S.k_full[ks], kTile);
                 for (int b = 0; b < 2; ++b)
                     tma_load_3d(S.k[ks] + b * kBox, &tmK, 64 * b, j * kBP, h, &S.k_full[ks], pol_kv);
-                issued_k = j + 1;
+                issued = j + 1;
+            }
+            if (!ok) {
+                // the copies still in flight land before the CTA may exit (bounded waits)
+                for (int j = issued - kKS; j < issued; ++j)
+                    if (j >= 0) mbar_wait(&S.k_full[j % kKS], (j / kKS) & 1u);
+                mbar_wait(&S.q_full, 0);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kVWarp) {
+        if (lane == 0) {
+            uint64_t pol_kv;
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_kv));
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+            pdl_wait();  // V may be written by earlier kernels in the stream
+            int issued = 0;
+            for (int j = 0; j < nkv && ok; ++j) {
+                const int vs = j % kVS;
                 if (j >= kVS && !mbar_wait(&S.v_empty[vs], ((j / kVS) - 1) & 1u)) { ok = false; break; }
                 mbar_expect_tx(&S.v_full[vs], kTile);
                 for (int b = 0; b < 2; ++b)
                     tma_load_3d(S.v[vs] + b * kBox, &tmV, 64 * b, j * kBP, h, &S.v_full[vs], pol_kv);
-                issued_v = j + 1;
+                issued = j + 1;
             }
             if (!ok) {
-                // the copies still in flight land before the CTA may exit (bounded waits)
-                for (int j = issued_k - kKS; j < issued_k; ++j)
-                    if (j >= 0) mbar_wait(&S.k_full[j % kKS], (j / kKS) & 1u);
-                for (int j = issued_v - kVS; j < issued_v; ++j)
+                for (int j = issued - kVS; j < issued; ++j)
                     if (j >= 0) mbar_wait(&S.v_full[j % kVS], (j / kVS) & 1u);
-                mbar_wait(&S.q_full, 0);
             }
         }
         __syncwarp();
@@ -334,7 +353,9 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         const float cs = a.scale_log2;
         const uint64_t cs2 = f2_pack(cs, cs);
         float m = -INFINITY;
-        uint64_t l2 = 0ull;  // two partial sums of the row's probabilities (fp32 pair)
+        // four partial sums of the row's probabilities (two fp32 pairs, so that the
+        // additions of a tile form two independent chains)
+        uint64_t l2 = 0ull, l2b = 0ull;
         if (!a.first) {  // the state of the earlier windows: m, and l in half 0's sum
             pdl_wait();  // written by the window before, maybe still running
             m = a.state[srow * kStateStride];
@@ -359,9 +380,11 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 for (int c = 0; c < 64; ++c)
                     if (c > last) sv[c >> 5][c & 31] = 0xff800000u;
             }
-            float mx = -INFINITY;
+            // tile maximum as four independent chains of 16
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(sv[c >> 5][c & 31]));
+            for (int c = 0; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], __uint_as_float(sv[c >> 5][c & 31]));
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             S.red[sb][hf][r] = mx;
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.pair_max[sb][qd]);
@@ -384,6 +407,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 }
                 const uint64_t al2 = f2_pack(alpha, alpha);
                 asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(l2) : "l"(al2));
+                asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(l2b) : "l"(al2));
             } else if (j > 0 && __any_sync(WSW_FULL_MASK, raise)) {
                 // O must hold P_{j-1} V_{j-1} before it is rescaled
                 if (!__all_sync(WSW_FULL_MASK, mbar_wait(&S.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1u))) {
@@ -410,6 +434,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                     tmem_st32(lane_base + kColO + 64 * hf + 32 * c, o);
                 }
                 asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(l2) : "l"(al2));
+                asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(l2b) : "l"(al2));
             }
             if (raise) m = mt;
             // P_j into its tensor-memory slot, free once P_{j-2} V_{j-2} has completed
@@ -430,7 +455,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 const float p0 = ex2(t0), p1 = ex2(t1);
                 const __half2 hp = __floats2half2_rn(p0, p1);
                 pk[i] = *reinterpret_cast<const uint32_t *>(&hp);
-                asm("add.rn.f32x2 %0, %0, %1;" : "+l"(l2) : "l"(f2_pack(p0, p1)));
+                if (i & 1) asm("add.rn.f32x2 %0, %0, %1;" : "+l"(l2b) : "l"(f2_pack(p0, p1)));
+                else asm("add.rn.f32x2 %0, %0, %1;" : "+l"(l2) : "l"(f2_pack(p0, p1)));
             }
             tmem_st32(lane_base + kColP + 64 * sb + 32 * hf, pk);
             tmem_wait_st();
@@ -439,9 +465,10 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             if (lane == 0) mbar_arrive(&S.p_full[sb]);
         }
         // epilogue: the row sum from both halves, then this half of O / l
-        float l0, l1;
+        float l0, l1, l2f, l3;
         f2_unpack(l2, l0, l1);
-        S.lsum[hf][r] = l0 + l1;
+        f2_unpack(l2b, l2f, l3);
+        S.lsum[hf][r] = (l0 + l1) + (l2f + l3);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.pair_sum[qd]);
         const bool have = __all_sync(WSW_FULL_MASK, ok && mbar_wait(&S.pair_sum[qd], 0) && mbar_wait(&S.o_final, 0));

@@ -12,11 +12,14 @@
 //    walked in stages of one or two 64-element boxes (128 bytes of bf16 = one 128-byte
 //    swizzle row per box); the memory-bound small-NT tiles take two, so that 256
 //    consecutive bytes of each weight row are requested together.
-//  * Warp 0 streams W and X blocks with cp.async.bulk.tensor (TMA) into a ring of
-//    shared-memory stages guarded by mbarriers; warp 1 allocates tensor memory and one
-//    of its threads issues tcgen05.mma (M = 128, N = NT, K = 16, bf16 in, fp32
-//    accumulate) and tcgen05.commit to release stages; warps 2-5 are the epilogue,
-//    reading the accumulator with tcgen05.ld (each warp owns its 32 tensor-memory lanes).
+//  * Warp 0 streams W boxes and warp 2 X boxes with cp.async.bulk.tensor (TMA) into a
+//    ring of shared-memory stages guarded by mbarriers.  Two issuing threads, because on
+//    GB300 a thread that issues a TMA tile load is held for about 550 cycles whatever the
+//    box size: one thread issuing both boxes of a stage took twice as long per stage as
+//    the MMAs of a 128 x 256 tile.  Warp 1 allocates tensor memory and one of its threads
+//    issues tcgen05.mma (M = 128, N = NT, K = 16, bf16 in, fp32 accumulate) and
+//    tcgen05.commit to release stages; warps 2-5 are the epilogue, reading the
+//    accumulator with tcgen05.ld (each warp owns its 32 tensor-memory lanes).
 //  * Tiles are few (20 for a 2560-row weight at NT <= 256), so K is split over a
 //    thread-block cluster of S CTAs (S chosen on the host from the cluster occupancy):
 //    each CTA accumulates its share of K, writes the partial tile to its own shared
@@ -107,69 +110,86 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    bool ok = true;
 
     if (warp == 0) {
         if (lane == 0) {
-            uint64_t pol_w, pol_x;
+            // W: stage i's boxes (consecutive 128-byte pieces of each weight row, requested
+            // back to back); this thread also arms full[i % stages] with the bytes of W and
+            // X.  The weights do not come from earlier kernels, so the first ring of W
+            // stages is in flight before anything waits for the previous kernel.
+            uint64_t pol_w;
             asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
-            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
-            // stage i: W boxes (consecutive 128-byte pieces of each weight row, requested
-            // back to back) and X boxes, both counted by full[i % stages]
-            auto load_w = [&](int i) {
-                const int s = i % stages, k = (kb0 + i) * kAtom * atoms;
-                for (int j = 0; j < atoms; ++j)
-                    tma_load_2d(sA + static_cast<size_t>(s) * a_bytes + j * kAtomA, &tmW, k + j * kAtom,
-                                static_cast<int>(m0), &full[s], pol_w);
-            };
-            auto load_x = [&](int i) {
-                const int s = i % stages, k = (kb0 + i) * kAtom * atoms;
-                for (int j = 0; j < atoms; ++j)
-                    tma_load_2d(sB + static_cast<size_t>(s) * b_bytes + j * (nt * kAtom * 2), &tmX, k + j * kAtom, n0,
-                                &full[s], pol_x);
-            };
-            // The weights do not come from earlier kernels: the first ring of W stages is
-            // in flight before the dependency wait, X (written by earlier kernels) after it.
-            const int pre = nk < stages ? nk : stages;
-            for (int i = 0; i < pre; ++i) {
-                mbar_expect_tx(&full[i], a_bytes + b_bytes);
-                load_w(i);
-            }
-            pdl_wait();
-            for (int i = 0; i < pre; ++i) load_x(i);
-            for (int i = pre; i < nk && ok; ++i) {
-                const int s = i % stages;
-                const uint32_t round = static_cast<uint32_t>(i / stages);
-                if (!mbar_wait(&empty[s], (round & 1u) ^ 1u)) { ok = false; break; }
+            uint32_t s = 0, phase = 0;
+            for (int i = 0; i < nk; ++i) {
+                if (i >= stages && !mbar_wait(&empty[s], phase ^ 1u)) break;
                 mbar_expect_tx(&full[s], a_bytes + b_bytes);
-                load_w(i);
-                load_x(i);
+                const int k = (kb0 + i) * kAtom * atoms;
+                for (int j = 0; j < atoms; ++j)
+                    tma_load_2d(sA + s * a_bytes + j * kAtomA, &tmW, k + j * kAtom, static_cast<int>(m0), &full[s],
+                                pol_w);
+                if (++s == static_cast<uint32_t>(stages)) {
+                    s = 0;
+                    phase ^= 1u;
+                }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
+            // One thread keeps the tensor core fed, so its loop is kept short: the stage
+            // and its phase advance by counting, and the descriptors of stage s are the
+            // stage-0 descriptors plus s stage sizes (start addresses are in 16-byte units
+            // and stay inside the 14-bit field: shared memory is below 256 KB).
             const uint32_t idesc = instr_desc(kBM, nt);
-            for (int i = 0; i < nk && ok; ++i) {
-                const int s = i % stages;
-                const uint32_t round = static_cast<uint32_t>(i / stages);
-                if (!mbar_wait(&full[s], round & 1u)) { ok = false; break; }
+            const uint64_t da0 = sw128_desc(saddr(sA)), db0 = sw128_desc(saddr(sB));
+            const uint32_t a_stage = a_bytes >> 4, b_stage = b_bytes >> 4;
+            const uint32_t a_box = kAtomA >> 4, b_box = (static_cast<uint32_t>(nt) * kAtom * 2) >> 4;
+            uint32_t s = 0, phase = 0;
+            for (int i = 0; i < nk; ++i) {
+                if (!mbar_wait(&full[s], phase)) break;
                 tc_fence_after();
-                for (int j = 0; j < atoms; ++j) {
-                    const uint64_t da = sw128_desc(saddr(sA + static_cast<size_t>(s) * a_bytes + j * kAtomA));
-                    const uint64_t db = sw128_desc(saddr(sB + static_cast<size_t>(s) * b_bytes + j * (nt * kAtom * 2)));
+                const uint64_t da = da0 + s * a_stage, db = db0 + s * b_stage;
+                if (atoms == 1) {
 #pragma unroll
                     for (int kk = 0; kk < kAtom / 16; ++kk)  // K = 16 per MMA: +32 bytes within the atom
-                        mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (i | j | kk) != 0);
+                        mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (i | kk) != 0);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int kk = 0; kk < kAtom / 16; ++kk)
+                            mma_bf16(tmem, da + j * a_box + 2 * kk, db + j * b_box + 2 * kk, idesc, (i | j | kk) != 0);
                 }
                 mma_commit(&empty[s]);
+                if (++s == static_cast<uint32_t>(stages)) {
+                    s = 0;
+                    phase ^= 1u;
+                }
             }
             mma_commit(accum);
         }
         __syncwarp();
     } else {
+        if (warp == 2 && lane == 0) {
+            // X: written by earlier kernels, so after the dependency wait
+            uint64_t pol_x;
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+            pdl_wait();
+            uint32_t s = 0, phase = 0;
+            for (int i = 0; i < nk; ++i) {
+                if (i >= stages && !mbar_wait(&empty[s], phase ^ 1u)) break;
+                const int k = (kb0 + i) * kAtom * atoms;
+                for (int j = 0; j < atoms; ++j)
+                    tma_load_2d(sB + s * b_bytes + j * (nt * kAtom * 2), &tmX, k + j * kAtom, n0, &full[s], pol_x);
+                if (++s == static_cast<uint32_t>(stages)) {
+                    s = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
         // epilogue: warp w owns tensor-memory lanes 32*(w % 4) .. +31 = tile rows
         const int q = warp & 3;
         const int row = 32 * q + lane;
