@@ -1010,6 +1010,7 @@ def profile_case(argv):
         python bench.py --profile-case gemm_bf16 [N]
         python bench.py --profile-case dequant_kv [depth]
         python bench.py --profile-case moe [T [gate_up|down]]
+        python bench.py --profile-case moe_repeat
         python bench.py --profile-case quantize [n block]
         python bench.py --profile-case attn_decode [depth group]
         python bench.py --profile-case attn_prefill [depth]
@@ -1072,6 +1073,18 @@ def profile_case(argv):
         xd = torch.rand((T * MOE_TOPK, Kx // 32), device=dev, generator=g).half()
         for _ in range(launches):
             wsw.moe_gemv_q8_0(Wq, Wd, xq, xd, ids)
+    elif what == "moe_repeat":
+        # the gathered form (16 routed rows) with each of 8 experts routed twice; two
+        # weight copies alternate, so a call finds none of its experts in L2
+        E, Mo, Kx = MOE_E, 2 * MOE_F, MOE_H
+        W = [(torch.randint(-127, 128, (E, Mo, Kx), dtype=torch.int8, device=dev, generator=g),
+              (torch.rand((E, Mo, Kx // 32), device=dev, generator=g) * 1e-3).half()) for _ in range(2)]
+        ids = torch.tensor([3, 17, 3, 40, 17, 99, 40, 5, 99, 64, 5, 64, 120, 7, 120, 7], dtype=torch.int32,
+                           device=dev)
+        xq = torch.randint(-127, 128, (16, Kx), dtype=torch.int8, device=dev, generator=g)
+        xd = torch.rand((16, Kx // 32), device=dev, generator=g).half()
+        for i in range(launches):
+            wsw.moe_gemv_q8_0(W[i % 2][0], W[i % 2][1], xq, xd, ids)
     elif what == "attn_decode":
         D = int(argv[1]) if len(argv) > 1 else 32768
         G = int(argv[2]) if len(argv) > 2 else 1
