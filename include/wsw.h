@@ -242,9 +242,10 @@ size_t wsw_moe_workspace_bytes(int64_t E, int64_t K, int64_t R);
  * For each row m < R with e = ids[m] in [0, E):
  *   y[m][o] = gemv_q8_0(W_e, x_m)[o],  o < Mo,
  * bit-identical to wsw_gemv_q8_0 on expert e's matrix and row m for R <= 256.
- * Each expert that some row uses is streamed from memory once per call (for R <= 16
- * each routed row streams its own expert, so a repeated expert is read again);
- * experts no row uses are not read.  For R > 256 with a workspace, a prepass sorts
+ * Each expert that some row uses is streamed from DRAM once per call; experts no row
+ * uses are not read.  (For R <= 16 each routed row streams its own expert's rows; a
+ * repeated expert's second pass is served by L2 while the routed experts' weights fit
+ * in it, as they do for 16 rows of 128 x 1536 x 2048 experts.)  For R > 256 with a workspace, a prepass sorts
  * and converts the activations into the workspace and the rows of an expert are
  * multiplied on the tensor cores with exact integer block sums; results then agree
  * with the CUDA-core form within fp32 rounding, not bit for bit.
