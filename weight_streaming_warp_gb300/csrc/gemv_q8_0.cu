@@ -210,8 +210,7 @@ struct Q8X : Q8 {
 // dense mat-vec over R * Mo virtual rows, virtual row v = m * Mo + o multiplying row o of
 // expert ids[m] with activation row m, so that y[m][o] = y[v] in the caller's [R][Mo]
 // layout.  Nothing is bucketed: every routed row streams its expert's rows (a repeated
-// expert among so few rows is streamed again, and L2 serves that pass while the routed
-// experts fit in it).  The weight addresses come from the ids, which
+// expert among so few rows is read again).  The weight addresses come from the ids, which
 // an earlier kernel writes, so the dependency wait comes first (kWaitFirst).  The rows per
 // warp divide Mo and the K-segments are the dense model's for one Mo x K matrix, so every
 // row equals wsw_gemv_q8_0 on its expert, bit for bit.
