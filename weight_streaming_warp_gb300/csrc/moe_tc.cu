@@ -499,34 +499,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            // This thread's loop is the kernel's issue bottleneck, so every ring position
+            // advances by counting (no division or modulo per stage) and the B descriptors
+            // are a base plus the slot's offset.  Stage g (counted across items) uses A slot
+            // g % kAB, B slot g % kBS, accumulator pairs 2g and 2g + 1 (mod kDPairs) and
+            // barrier g % kDStageBars; the pair counter p1 = (2g + 1) mod 2 kDPairs gives
+            // both the pair and its phase.
+            static_assert(kAB == 2 && kDPairs == 3, "ring sizes");
+            const uint64_t bd0 = sw128_desc(saddr(S.bt[0]));
+            constexpr uint32_t kBSlot16 = kBBytes >> 4, kBAtom16 = kBAtom >> 4;
+            int v = 0, u = 0, dsb = 0, p1 = 1;
+            uint32_t pa = 0;  // A-slot phase
             for (int k = 0; k < my_items && ok; ++k) {
                 Item it;
                 decode_item(S, static_cast<int>(blockIdx.x) + k * C, ecur, it);
                 const uint32_t idesc = instr_desc(kRows, (it.n + 15) & ~15, false);
-                for (int s = 0; s < kst && ok; ++s) {
+                for (int s = 0; s < kst; ++s) {
                     // A full also means this stage's B tile has landed (the A converters
                     // wait for it), and the epilogue frees accumulator pairs in order, so
                     // one wait each covers the stage
-                    const int g = k * kst + s, v = g % kAB, u = g % kBS, gp1 = 2 * g + 1;
-                    if (!mbar_wait(&S.a_full[v], (g / kAB) & 1u) ||
-                        !mbar_wait(&S.d_empty[gp1 % kDPairs], ((gp1 / kDPairs) & 1u) ^ 1u)) {
+                    const int pair1 = p1 < kDPairs ? p1 : p1 - kDPairs;  // pair 2g + 1
+                    const uint32_t ph1 = p1 < kDPairs ? 0u : 1u;        // its round's parity
+                    const int pair0 = pair1 == 0 ? kDPairs - 1 : pair1 - 1;
+                    if (!mbar_wait(&S.a_full[v], pa) || !mbar_wait(&S.d_empty[pair1], ph1 ^ 1u)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t bd = sw128_desc(saddr(S.bt[u]));
+                    const uint64_t bd = bd0 + static_cast<uint32_t>(u) * kBSlot16;
                     const uint32_t at0 = tmem + kACol + static_cast<uint32_t>(64 * v);
+                    const uint32_t d0 = tmem + kDCol + static_cast<uint32_t>(128 * pair0);
+                    const uint32_t d1 = tmem + kDCol + static_cast<uint32_t>(128 * pair1);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {  // block j of the stage: pair 2 g + j / 2, slot half j % 2
-                        const uint32_t d = tmem + kDCol + static_cast<uint32_t>(128 * ((2 * g + (j >> 1)) % kDPairs) + 64 * (j & 1));
+                        const uint32_t d = (j < 2 ? d0 : d1) + static_cast<uint32_t>(64 * (j & 1));
                         // atom j / 2 of the B tile, bytes 64 (j % 2) + {0, 32} of its rows
-                        const uint64_t b0 = bd + static_cast<uint64_t>((j >> 1) * (kBAtom >> 4) + (j & 1) * 4);
+                        const uint64_t b0 = bd + static_cast<uint64_t>((j >> 1) * kBAtom16 + (j & 1) * 4);
                         mma_ts(d, at0 + 16 * j, b0, idesc, 0u);
                         mma_ts(d, at0 + 16 * j + 8, b0 + 2, idesc, 1u);
                     }
-                    mma_commit(&S.d_full[g % kDStageBars]);
+                    mma_commit(&S.d_full[dsb]);
                     mma_commit(&S.a_empty[v]);
                     mma_commit(&S.b_empty[u]);
+                    v ^= 1;
+                    if (v == 0) pa ^= 1u;
+                    if (++u == kBS) u = 0;
+                    if (++dsb == kDStageBars) dsb = 0;
+                    p1 += 2;
+                    if (p1 >= 2 * kDPairs) p1 -= 2 * kDPairs;
                 }
             }
         }
