@@ -275,33 +275,34 @@ __global__ void __launch_bounds__(kPrepThreads, 1) moe_q8_prep_kernel(const MoeT
     // behind the bucketing (whether a row is used is known only afterwards).
     const int m0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * R / gridDim.x);
     const int m1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * R / gridDim.x);
-    const int64_t chunks = a.K / 16;
-    const int64_t work = static_cast<int64_t>(m1 - m0) * chunks;
-    const int64_t swork = static_cast<int64_t>(m1 - m0) * (nb / 8);  // 8 binary16 scales a piece
+    // 32-bit piece indices: R <= kMaxRows and K / 16 <= 2 * kMaxBlocks
+    const uint32_t chunks = static_cast<uint32_t>(a.K / 16);
+    const uint32_t spr = static_cast<uint32_t>(nb / 8);  // scale pieces per row (8 binary16 a piece)
+    const uint32_t work = static_cast<uint32_t>(m1 - m0) * chunks;
+    const uint32_t swork = static_cast<uint32_t>(m1 - m0) * spr;
     constexpr int kPre = 8;
     uint4 pre[kPre], spre;
 #pragma unroll
     for (int u = 0; u < kPre; ++u) {
-        const int64_t w = threadIdx.x + static_cast<int64_t>(u) * kPrepThreads;
+        const uint32_t w = threadIdx.x + static_cast<uint32_t>(u) * kPrepThreads;
         if (w < work) {
-            const int64_t r = w / chunks;
+            const uint32_t r = w / chunks;
             pre[u] = __ldg(reinterpret_cast<const uint4 *>(a.xq + static_cast<int64_t>(m0 + r) * a.K) + (w - r * chunks));
         }
     }
     if (threadIdx.x < swork) {
-        const int64_t r = threadIdx.x / (nb / 8);
-        spre = __ldg(reinterpret_cast<const uint4 *>(a.xd + static_cast<int64_t>(m0 + r) * nb) +
-                     (threadIdx.x - r * (nb / 8)));
+        const uint32_t r = threadIdx.x / spr;
+        spre = __ldg(reinterpret_cast<const uint4 *>(a.xd + static_cast<int64_t>(m0 + r) * nb) + (threadIdx.x - r * spr));
     }
     __syncthreads();
     const int r0 = warp < kBucketWarps ? static_cast<int>(static_cast<int64_t>(warp) * R / kBucketWarps) : 0;
     const int r1 = warp < kBucketWarps ? static_cast<int>(static_cast<int64_t>(warp + 1) * R / kBucketWarps) : 0;
+    // per-warp counts of each expert (shared-memory atomics: a count does not depend on
+    // the order; __match_any_sync costs a pass per distinct expert of the 32 ids)
     for (int base = r0; base < r1; base += 32) {
         const int m = base + lane;
         const int e = m < r1 ? ids_s[m] : -1;
-        const unsigned peers = __match_any_sync(WSW_FULL_MASK, e >= 0 ? e : E + lane);
-        if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
-        __syncwarp();
+        if (e >= 0) atomicAdd(&wcnt[warp * E + e], 1);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kPrepThreads) {
@@ -347,13 +348,24 @@ __global__ void __launch_bounds__(kPrepThreads, 1) moe_q8_prep_kernel(const MoeT
         }
     }
     __syncthreads();
+    // stable positions: row m goes after the earlier rows of its expert in earlier warps
+    // (the warp base), in earlier chunks of this warp (the running count) and at lower
+    // lanes of its chunk (counted over the 32 lanes by shuffles)
     for (int base = r0; base < r1; base += 32) {
         const int m = base + lane;
         const int e = m < r1 ? ids_s[m] : -1;
-        const unsigned peers = __match_any_sync(WSW_FULL_MASK, e >= 0 ? e : E + lane);
-        if (e >= 0) pos[m] = off[e] + wcnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
+        int below = 0;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+            const int ej = __shfl_sync(WSW_FULL_MASK, e, j);
+            below += (j < lane) & (ej == e);
+        }
+        const int run = e >= 0 ? wcnt[warp * E + e] : 0;
         __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + e] += __popc(peers);
+        if (e >= 0) {
+            pos[m] = off[e] + run + below;
+            atomicAdd(&wcnt[warp * E + e], 1);
+        }
         __syncwarp();
     }
     __syncthreads();
@@ -365,8 +377,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) moe_q8_prep_kernel(const MoeT
     }
     // convert the preloaded pieces to fp16 at their sorted rows, then any remaining ones
     // (four loads in flight a pass)
-    auto put = [&](int64_t w, const uint4 &v) {
-        const int64_t r = w / chunks;
+    auto put = [&](uint32_t w, const uint4 &v) {
+        const uint32_t r = w / chunks;
         const int m = m0 + static_cast<int>(r);
         if (ids_s[m] < 0) return;
         uint32_t h[8];
@@ -377,39 +389,39 @@ __global__ void __launch_bounds__(kPrepThreads, 1) moe_q8_prep_kernel(const MoeT
     };
 #pragma unroll
     for (int u = 0; u < kPre; ++u) {
-        const int64_t w = threadIdx.x + static_cast<int64_t>(u) * kPrepThreads;
+        const uint32_t w = threadIdx.x + static_cast<uint32_t>(u) * kPrepThreads;
         if (w < work) put(w, pre[u]);
     }
-    for (int64_t w0 = threadIdx.x + static_cast<int64_t>(kPre) * kPrepThreads; w0 < work; w0 += 4 * kPrepThreads) {
+    for (uint32_t w0 = threadIdx.x + static_cast<uint32_t>(kPre) * kPrepThreads; w0 < work; w0 += 4 * kPrepThreads) {
         uint4 v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int64_t w = w0 + u * kPrepThreads;
+            const uint32_t w = w0 + u * kPrepThreads;
             if (w < work) {
-                const int64_t r = w / chunks;
+                const uint32_t r = w / chunks;
                 v[u] = __ldg(reinterpret_cast<const uint4 *>(a.xq + static_cast<int64_t>(m0 + r) * a.K) + (w - r * chunks));
             }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int64_t w = w0 + u * kPrepThreads;
+            const uint32_t w = w0 + u * kPrepThreads;
             if (w < work) put(w, v[u]);
         }
     }
     // scales: 8 per piece, fp32 at [block][sorted row]
-    auto put_scales = [&](int64_t w, const uint4 &v) {
-        const int64_t r = w / (nb / 8);
+    auto put_scales = [&](uint32_t w, const uint4 &v) {
+        const uint32_t r = w / spr;
         const int m = m0 + static_cast<int>(r);
         if (ids_s[m] < 0) return;
-        const int b0 = 8 * static_cast<int>(w - r * (nb / 8));
+        const int b0 = 8 * static_cast<int>(w - r * spr);
         const __half *hv = reinterpret_cast<const __half *>(&v);
 #pragma unroll
         for (int i = 0; i < 8; ++i) xs[static_cast<int64_t>(b0 + i) * L.Rp + pos[m]] = __half2float(hv[i]);
     };
     if (threadIdx.x < swork) put_scales(threadIdx.x, spre);
-    for (int64_t w = threadIdx.x + kPrepThreads; w < swork; w += kPrepThreads) {
-        const int64_t r = w / (nb / 8);
-        put_scales(w, __ldg(reinterpret_cast<const uint4 *>(a.xd + static_cast<int64_t>(m0 + r) * nb) + (w - r * (nb / 8))));
+    for (uint32_t w = threadIdx.x + kPrepThreads; w < swork; w += kPrepThreads) {
+        const uint32_t r = w / spr;
+        put_scales(w, __ldg(reinterpret_cast<const uint4 *>(a.xd + static_cast<int64_t>(m0 + r) * nb) + (w - r * spr)));
     }
 }
 
