@@ -7,8 +7,9 @@
 //
 // Every CTA buckets the routed rows by expert in shared memory (no global scratch):
 // the ids are read once, each warp counts the experts of its own chunk of rows with
-// __match_any_sync, per-expert bases follow from the per-warp counts, and a second pass
-// writes every expert's rows in row order (so all CTAs build the same lists).
+// shared-memory atomics, per-expert bases follow from the per-warp counts, and a second
+// pass writes every expert's rows in row order (ranks within 32 rows by shuffles), so
+// all CTAs build the same lists.
 //
 // Work units are (used expert e, a run of P row pairs of e's weights, batch j of up to
 // 4 of e's rows), ordered by expert, then by run, then by batch, so the batches of one
@@ -126,12 +127,12 @@ __global__ void __launch_bounds__(kT, 2) moe_cc_kernel(const MoeArgs a) {
     __syncthreads();
     const int r0 = static_cast<int>(static_cast<int64_t>(wid) * R / kW);
     const int r1 = static_cast<int>(static_cast<int64_t>(wid + 1) * R / kW);
+    // per-warp counts of each expert (shared-memory atomics: a count does not depend on
+    // the order; __match_any_sync costs a pass per distinct expert of the 32 ids)
     for (int base = r0; base < r1; base += 32) {
         const int m = base + lane;
         const int e = m < r1 ? ids_s[m] : -1;
-        const unsigned peers = __match_any_sync(WSW_FULL_MASK, e >= 0 ? e : E + lane);
-        if (e >= 0 && lane == __ffs(peers) - 1) wbase[wid * E + e] += __popc(peers);
-        __syncwarp();
+        if (e >= 0) atomicAdd(&wbase[wid * E + e], 1);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kT) {
@@ -180,13 +181,23 @@ __global__ void __launch_bounds__(kT, 2) moe_cc_kernel(const MoeArgs a) {
         }
     }
     __syncthreads();
+    // stable lists: row m goes after the earlier rows of its expert in earlier warps,
+    // earlier chunks of this warp and lower lanes of its chunk (counted by shuffles)
     for (int base = r0; base < r1; base += 32) {
         const int m = base + lane;
         const int e = m < r1 ? ids_s[m] : -1;
-        const unsigned peers = __match_any_sync(WSW_FULL_MASK, e >= 0 ? e : E + lane);
-        if (e >= 0) list[off[e] + wbase[wid * E + e] + __popc(peers & ((1u << lane) - 1u))] = m;
+        int below = 0;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+            const int ej = __shfl_sync(WSW_FULL_MASK, e, j);
+            below += (j < lane) & (ej == e);
+        }
+        const int run = e >= 0 ? wbase[wid * E + e] : 0;
         __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) wbase[wid * E + e] += __popc(peers);
+        if (e >= 0) {
+            list[off[e] + run + below] = m;
+            atomicAdd(&wbase[wid * E + e], 1);
+        }
         __syncwarp();
     }
     __syncthreads();
