@@ -119,8 +119,9 @@ def test_other_calls_reject_on_host(lib):
     assert c(0, None, None, None) == 0
     ab = lib.wsw_attn_decode_workspace_bytes
     # one partial (max, sum, 128 values) per (chunk, head, query); chunks of whole
-    # 64-position tiles, about 320 of them over all heads
-    assert ab(32768, 4, 8) == 74 * 4 * 8 * 130 * 4
+    # 16-position steps, about 152 of them over all heads
+    assert ab(32768, 4, 8) == 38 * 4 * 8 * 130 * 4
+    assert ab(65536, 1, 1) == 152 * 130 * 4
     assert ab(1, 4, 1) == 4 * 130 * 4
     assert ab(0, 4, 1) == 0 and ab(64, 4, 16) == 0
     a = lib.wsw_attn_decode_f16

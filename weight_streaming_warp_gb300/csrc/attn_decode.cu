@@ -11,24 +11,16 @@
 //   out[h][g][i] = sum_p exp(s_p - m) V(h, p)[i] / sum_p exp(s_p - m),  m = max_p s_p
 //
 // Design (GB300), flash decoding in two launches:
-//  * attn_decode_split_kernel: grid (splits, heads), 256 threads, two CTAs per SM.  A
-//    CTA takes a chunk of positions of one KV head for all G query heads of its group,
-//    so every K and V byte is read once per step.  Tiles of 64 positions of K and V
-//    (2 x 16 KB) are copied with 16-byte cp.async into a three-stage ring (two tiles in
-//    flight while one is used); the 16-byte chunks of odd rows are XOR-swizzled so that
-//    the reads below hit distinct banks.
-//      scores:  four lanes per position, each a quarter of the 128 dimensions, for all
-//               G queries at once (each K value is read from shared memory once),
-//               reduced with two xor shuffles; scores are kept in the log2 domain
-//               (scale * log2 e folded into q), so the weights are exp2f(s - m)
-//      softmax: warp g takes query g's 64 scores, the running maximum and the factor
-//               exp2f(m_old - m_new) that rescales what was accumulated so far
-//      values:  warp w takes every eighth position (w, w + 8, ...) for all G queries;
-//               a lane owns four dimensions, so a warp reads whole 256-byte V rows
-//    At the end of its chunk the CTA adds its warps' partial sums and writes
-//    (m, l = sum of weights, acc[128]) of each query to the workspace.
+//  * attn_decode_warp_kernel: grid (splits, heads) of about one CTA per SM, 256 threads.
+//    A CTA takes a chunk of positions of one KV head for all G query heads of its group,
+//    so every K and V byte is read once per step.  Each of its eight warps walks its own
+//    run of 16-position steps through a private three-stage cp.async ring and keeps its
+//    own online softmax, so the loop has no block barrier; the warps' partials are
+//    merged once at the end, and the CTA writes (m, l = sum of weights, acc[128]) of each
+//    query to the workspace.  Scores are kept in the log2 domain (scale * log2 e folded
+//    into q), so the weights are exp2f(s - m).
 //  * attn_decode_combine_kernel (PDL-linked): one CTA per (head, query); rescales every
-//    chunk's partials to the global maximum, adds them in a fixed order and divides, so
+//    chunk's partials to a common maximum, adds them in a fixed order and divides, so
 //    the result does not depend on the launch.
 //  * The dot products and the value sums use packed fp32x2 FMAs (even and odd
 //    dimensions in the two lanes), which halves their instruction count.
@@ -44,12 +36,8 @@ namespace wsw {
 namespace {
 
 constexpr int kDh = 128;                // head_dim
-constexpr int kTile = 64;               // positions per tile
 constexpr int kThreads = 256;           // 8 warps
 constexpr int kRowBytes = kDh * 2;      // one K or V row in shared memory
-constexpr int kTileBytes = kTile * kRowBytes;
-constexpr int kStages = 3;              // tiles in the ring: two in flight while one is used
-constexpr int kTargetCtas = 320;        // about two CTAs per SM on a 152-SM part
 constexpr int kPart = kDh + 2;          // floats per (chunk, head, query): m, l, acc
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -58,18 +46,13 @@ struct AttnArgs {
     const __half *k, *v;
     int64_t depth, kps, khs, vps, vhs;  // strides in elements
     float qscale;                       // scale * log2(e)
-    int chunk;                          // positions per CTA (multiple of kTile)
+    int chunk;                          // positions per CTA (whole 16-position steps)
     int splits;
     int heads;
     float *ws;
     float *out;
 };
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                 "l"(src)
-                 : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -96,258 +79,295 @@ __device__ __forceinline__ uint64_t h2_to_f2(uint32_t h) {
     return f2(f.x, f.y);
 }
 
-// Byte offset of 16-byte chunk c (0..15) of row r in a tile: bit 2 of the chunk index
-// flips on odd rows.  The score pass reads 16-byte chunks, a quarter-warp at a time: two
-// rows, four chunks each, which land on eight distinct chunk positions of 128 bytes,
-// i.e. distinct banks.  The value pass reads 8 bytes a lane, a half-warp at a time: one
-// row's 128 bytes, whose chunks the swizzle only permutes.
-__device__ __forceinline__ int chunk_off(int r, int c) { return r * kRowBytes + ((c ^ ((r & 1) << 2)) << 4); }
+// Warp-streaming form: each of the eight warps walks its own run of whole 16-position
+// steps of the CTA's chunk through a private three-stage cp.async ring (8 KB a stage:
+// 16 K rows, then 16 V rows), and keeps its own running maximum, weight sum and value
+// sums; the loop has no block barrier.  A lane copies, and later reads, only its own
+// 16-byte pieces: half-warp hf holds rows hf, hf + 2, ..., piece c = lane % 16 of each
+// row (dimensions 8 c .. 8 c + 7), so no lane waits on another lane's copies.
+//   scores:  the lane's partial dots with its eight rows, summed over the half-warp by a
+//            butterfly that halves the values in flight at each of its four shuffles
+//            (8 shuffles for 8 rows); lanes 2 i and 2 i + 1 of half hf end with the
+//            score of row 2 i + hf
+//   softmax: the step's maximum over the warp, then each lane's weight exp2(s - m)
+//   values:  each row's weight is shuffled from the lane that holds it
+// At the end the warps' partials are merged once in shared memory (one barrier) and the
+// CTA writes the same (m, l, acc) record as the tile form, for the same combine launch.
+constexpr int kWBatch = 16;                                // positions per warp step
+constexpr int kWStages = 3;
+constexpr int kWWarps = kThreads / 32;
+constexpr int kWStageBytes = 2 * kWBatch * kRowBytes;       // K and V rows of one step
+constexpr int kWSmem = kWWarps * kWStages * kWStageBytes;   // 192 KB: one CTA per SM
+constexpr int kWTargetCtas = 152;                          // one CTA per SM of a 152-SM part
+constexpr int kRed = kDh + 4;  // floats per warp partial in the merge: m, l, 2 pad, acc (16-byte aligned)
+
+// 16-byte copy that writes zeros and reads nothing when !valid (src must still be mapped)
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
 
 template <int G>
-__global__ void __launch_bounds__(kThreads, 2) attn_decode_split_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) attn_decode_warp_kernel(const AttnArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
-    unsigned char *kt = smem;                            // [kStages][kTile][kRowBytes]
-    unsigned char *vt = smem + kStages * kTileBytes;     // [kStages][kTile][kRowBytes]
-    float *qs = reinterpret_cast<float *>(smem + 2 * kStages * kTileBytes);  // [G][kDh], log2 domain
-    float *sw = qs + G * kDh;                  // [G][kTile] scores; weights then [kTile][G]
-    float *wt = sw + G * kTile;                // [kTile][G] weights
-    float *mrun = wt + G * kTile;              // [G] running maximum
-    float *alpha = mrun + G;                   // [G] rescale factor of the current tile
-
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int hf = lane >> 4, c = lane & 15;
     const int h = blockIdx.y;
     const int64_t p0 = static_cast<int64_t>(blockIdx.x) * a.chunk;
-    const int64_t p1 = p0 + a.chunk < a.depth ? p0 + a.chunk : a.depth;
-    const int ntiles = static_cast<int>((p1 - p0 + kTile - 1) / kTile);
+    const int64_t pend = p0 + a.chunk < a.depth ? p0 + a.chunk : a.depth;
+    const int nb = a.chunk / kWBatch;  // steps in a chunk; warp w takes [w nb / 8, (w + 1) nb / 8)
+    const int64_t w0 = p0 + static_cast<int64_t>(warp * nb / kWWarps) * kWBatch;
+    const int64_t wl = p0 + static_cast<int64_t>((warp + 1) * nb / kWWarps) * kWBatch;
+    const int64_t w1 = wl < pend ? wl : pend;
+    const int nsteps = w1 > w0 ? static_cast<int>((w1 - w0 + kWBatch - 1) / kWBatch) : 0;
     const __half *kh = a.k + h * a.khs, *vh = a.v + h * a.vhs;
+    unsigned char *ring = smem + warp * (kWStages * kWStageBytes);
 
-    // the first tile's lines into L2 before the dependency wait (L2 is the point of
+    // the first two steps' lines into L2 before the dependency wait (L2 is the point of
     // coherence, so this is safe while an earlier kernel may still write them)
-    {
-        const int r = tid >> 2, part = tid & 3;  // 64 rows x (2 lines of K, 2 of V)
-        if (p0 + r < p1) {
-            const __half *base = part < 2 ? kh + (p0 + r) * a.kps : vh + (p0 + r) * a.vps;
-            prefetch_l2(base + 64 * (part & 1));
-        }
+    for (int j = lane; j < 2 * 4 * kWBatch; j += 32) {
+        const int64_t p = w0 + (j >> 2);
+        if (p < w1) prefetch_l2(((j & 2) ? vh + p * a.vps : kh + p * a.kps) + 64 * (j & 1));
     }
     pdl_wait();
 
-    auto load_tile = [&](int t) {
-        if (t < ntiles) {
-            const int st = t % kStages;
-            const int64_t pb = p0 + static_cast<int64_t>(t) * kTile;
-            for (int i = tid; i < kTile * 16; i += kThreads) {
-                const int r = i >> 4, c = i & 15;
-                if (pb + r < p1) {
-                    cp_async16(kt + st * kTileBytes + chunk_off(r, c), kh + (pb + r) * a.kps + c * 8);
-                    cp_async16(vt + st * kTileBytes + chunk_off(r, c), vh + (pb + r) * a.vps + c * 8);
-                }
+    int ist = 0;  // ring stage of the next step to copy
+    auto issue = [&](int t) {
+        if (t < nsteps) {
+            unsigned char *stg = ring + ist * kWStageBytes;
+            const int64_t pb = w0 + static_cast<int64_t>(t) * kWBatch;
+#pragma unroll
+            for (int i = 0; i < kWBatch / 2; ++i) {
+                const int r = 2 * i + hf;
+                const bool ok = pb + r < w1;
+                const int64_t p = ok ? pb + r : w0;
+                cp_async16_zfill(stg + r * kRowBytes + c * 16, kh + p * a.kps + c * 8, ok);
+                cp_async16_zfill(stg + (kWBatch + r) * kRowBytes + c * 16, vh + p * a.vps + c * 8, ok);
             }
+            if (++ist == kWStages) ist = 0;
         }
-        cp_async_commit();  // one group per tile, empty past the end
+        cp_async_commit();  // one group per step, empty past the end
     };
-    load_tile(0);
-    load_tile(1);
-    // q after the first tiles' copies are on their way (its load would hold them up)
-    for (int i = tid; i < G * kDh; i += kThreads) qs[i] = a.q[static_cast<int64_t>(h) * G * kDh + i] * a.qscale;
-    if (tid < G) mrun[tid] = -INFINITY;
-    pdl_launch_dependents();
+    issue(0);
+    issue(1);
 
-    // value pass: this thread's dimensions 4 lane .. 4 lane + 3 for every query, over the
-    // positions warp, warp + 8, ... of each tile
-    uint64_t acc[G][2];
-    float l[G];
+    // this lane's eight dimensions of every query, in the log2 domain
+    uint64_t qv[G][4];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        acc[g][0] = acc[g][1] = 0ull;
-        l[g] = 0.f;
+        const float *qp = a.q + (static_cast<int64_t>(h) * G + g) * kDh + c * 8;  // 4-byte aligned
+#pragma unroll
+        for (int k = 0; k < 4; ++k) qv[g][k] = f2(qp[2 * k] * a.qscale, qp[2 * k + 1] * a.qscale);
     }
+    pdl_launch_dependents();
 
-    for (int t = 0; t < ntiles; ++t) {
-        const int st = t % kStages;
-        load_tile(t + 2);  // into the stage that tile t - 1 used
-        const int64_t left = p1 - (p0 + static_cast<int64_t>(t) * kTile);
-        const int nv = left < kTile ? static_cast<int>(left) : kTile;
+    float m[G], l[G];
+    uint64_t acc[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+        acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0ull;
+    }
+    const bool b3 = c & 8, b2 = c & 4, b1 = c & 2;
+    const int row = 2 * (c >> 1) + hf;  // the row whose score this lane ends with
+
+    int rst = 0;  // ring stage of the step being used
+    for (int t = 0; t < nsteps; ++t) {
+        issue(t + 2);
         cp_async_wait<2>();
-        __syncthreads();
-        // scores: position p = tid / 4, chunks 4 j + sub (dimensions 8 c .. 8 c + 7),
-        // j = 0..3; even and odd dimensions in the two lanes of a packed accumulator
-        {
-            const int p = tid >> 2, sub = tid & 3;
-            uint64_t d[G];
+        const unsigned char *stg = ring + rst * kWStageBytes;
+        if (++rst == kWStages) rst = 0;
+        const bool valid = w0 + static_cast<int64_t>(t) * kWBatch + row < w1;
+
+        uint64_t kf[kWBatch / 2][4];
 #pragma unroll
-            for (int g = 0; g < G; ++g) d[g] = 0ull;
-            const unsigned char *ktile = kt + st * kTileBytes;
+        for (int i = 0; i < kWBatch / 2; ++i) {
+            const uint4 kv = *reinterpret_cast<const uint4 *>(stg + (2 * i + hf) * kRowBytes + c * 16);
+            kf[i][0] = h2_to_f2(kv.x);
+            kf[i][1] = h2_to_f2(kv.y);
+            kf[i][2] = h2_to_f2(kv.z);
+            kf[i][3] = h2_to_f2(kv.w);
+        }
+        float w[G];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = 4 * j + sub;
-                const uint4 kv = *reinterpret_cast<const uint4 *>(ktile + chunk_off(p, c));
-                const uint64_t k01 = h2_to_f2(kv.x), k23 = h2_to_f2(kv.y), k45 = h2_to_f2(kv.z), k67 = h2_to_f2(kv.w);
+        for (int g = 0; g < G; ++g) {
+            float d[kWBatch / 2];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const ulonglong2 qa = *reinterpret_cast<const ulonglong2 *>(qs + g * kDh + c * 8);
-                    const ulonglong2 qb = *reinterpret_cast<const ulonglong2 *>(qs + g * kDh + c * 8 + 4);
-                    fma2(d[g], qa.x, k01);
-                    fma2(d[g], qa.y, k23);
-                    fma2(d[g], qb.x, k45);
-                    fma2(d[g], qb.y, k67);
-                }
+            for (int i = 0; i < kWBatch / 2; ++i) {
+                uint64_t x = 0ull;
+                fma2(x, qv[g][0], kf[i][0]);
+                fma2(x, qv[g][1], kf[i][1]);
+                fma2(x, qv[g][2], kf[i][2]);
+                fma2(x, qv[g][3], kf[i][3]);
+                d[i] = f2_sum(x);
             }
+            // butterfly over the half-warp: after the shuffle at distance 8 a lane keeps
+            // rows 0..3 or 4..7 (by bit 3 of c), at 4 two of those, at 2 one, and the
+            // shuffle at 1 completes the sum
+            float e4[4], e2[2];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float send = b3 ? d[k] : d[k + 4], keep = b3 ? d[k + 4] : d[k];
+                e4[k] = keep + __shfl_xor_sync(WSW_FULL_MASK, send, 8);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float send = b2 ? e4[k] : e4[k + 2], keep = b2 ? e4[k + 2] : e4[k];
+                e2[k] = keep + __shfl_xor_sync(WSW_FULL_MASK, send, 4);
+            }
+            const float send = b1 ? e2[0] : e2[1], keep = b1 ? e2[1] : e2[0];
+            const float e1 = keep + __shfl_xor_sync(WSW_FULL_MASK, send, 2);
+            float s = e1 + __shfl_xor_sync(WSW_FULL_MASK, e1, 1);
+            if (!valid) s = -INFINITY;
+            // online softmax: the step's maximum over the warp (lane pairs hold equal scores)
+            float mt = s;
+#pragma unroll
+            for (int off = 2; off <= 16; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(WSW_FULL_MASK, mt, off));
+            const float mn = fmaxf(m[g], mt);
+            const bool none = mn == -INFINITY;
+            const float al = none ? 1.f : exp2f(m[g] - mn);
+            w[g] = none ? 0.f : exp2f(s - mn);
+            m[g] = mn;
+            l[g] = l[g] * al + w[g];
+            const uint64_t al2 = f2(al, al);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(acc[g][k]) : "l"(al2));
+        }
+        // values: row 2 i + hf, piece c; its weight sits in lane 16 hf + 2 i
+#pragma unroll
+        for (int i = 0; i < kWBatch / 2; ++i) {
+            const uint4 vv = *reinterpret_cast<const uint4 *>(stg + (kWBatch + 2 * i + hf) * kRowBytes + c * 16);
+            const uint64_t v01 = h2_to_f2(vv.x), v23 = h2_to_f2(vv.y), v45 = h2_to_f2(vv.z), v67 = h2_to_f2(vv.w);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float e = f2_sum(d[g]);
-                e += __shfl_xor_sync(WSW_FULL_MASK, e, 1);
-                e += __shfl_xor_sync(WSW_FULL_MASK, e, 2);
-                if (sub == 0) sw[g * kTile + p] = p < nv ? e : -INFINITY;
+                const float wi = __shfl_sync(WSW_FULL_MASK, w[g], (lane & 16) | (2 * i));
+                const uint64_t w2 = f2(wi, wi);
+                fma2(acc[g][0], w2, v01);
+                fma2(acc[g][1], w2, v23);
+                fma2(acc[g][2], w2, v45);
+                fma2(acc[g][3], w2, v67);
             }
         }
-        __syncthreads();
-        // softmax of the tile: warp g handles query g; weights go out position-major
-        if (warp < G) {
-            const float *s = sw + warp * kTile;
-            const float s0 = s[lane], s1 = s[lane + 32];
-            float mt = fmaxf(s0, s1);
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(WSW_FULL_MASK, mt, off));
-            const float mo = mrun[warp];
-            const float mn = fmaxf(mo, mt);
-            const bool none = mn == -INFINITY;  // nothing seen yet: no weight, nothing to rescale
-            wt[lane * G + warp] = none ? 0.f : exp2f(s0 - mn);
-            wt[(lane + 32) * G + warp] = none ? 0.f : exp2f(s1 - mn);
-            if (lane == 0) {
-                alpha[warp] = none ? 1.f : exp2f(mo - mn);
-                mrun[warp] = mn;
-            }
-        }
-        __syncthreads();
-        // values: positions warp, warp + 8, ... of the tile, every query
-        {
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float al = alpha[g];
-                const uint64_t al2 = f2(al, al);
-                l[g] *= al;
-                asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(acc[g][0]) : "l"(al2));
-                asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(acc[g][1]) : "l"(al2));
-            }
-            const unsigned char *vtile = vt + st * kTileBytes;
-            for (int p = warp; p < nv; p += 8) {
-                const uint2 raw = *reinterpret_cast<const uint2 *>(vtile + chunk_off(p, lane >> 1) + (lane & 1) * 8);
-                const uint64_t v01 = h2_to_f2(raw.x), v23 = h2_to_f2(raw.y);
-                float w[G];
-#pragma unroll
-                for (int g4 = 0; g4 < (G + 3) / 4; ++g4) {
-                    if constexpr (G >= 4) {
-                        const float4 w4 = *reinterpret_cast<const float4 *>(wt + p * G + 4 * g4);
-                        w[4 * g4] = w4.x;
-                        w[4 * g4 + 1] = w4.y;
-                        w[4 * g4 + 2] = w4.z;
-                        w[4 * g4 + 3] = w4.w;
-                    } else {
-#pragma unroll
-                        for (int g = 0; g < G; ++g) w[g] = wt[p * G + g];
-                    }
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const uint64_t w2 = f2(w[g], w[g]);
-                    l[g] += w[g];
-                    fma2(acc[g][0], w2, v01);
-                    fma2(acc[g][1], w2, v23);
-                }
-            }
-        }
-        __syncthreads();  // stage st is free for tile t + 3
     }
     cp_async_wait<0>();
 
-    // add the eight warps' partials (in warp order) into the workspace
-    float *red = reinterpret_cast<float *>(smem);  // [8 warps][G][kDh + 1]; the tiles are done
-    __syncthreads();
+    // the warp's partial: the two half-warps' value sums added, the weight sum over the
+    // lanes of one parity of each pair (pairs hold equal weights)
+    __syncthreads();  // every warp is past its ring: it becomes the merge area
+    float *red = reinterpret_cast<float *>(smem);  // [8 warps][G][kRed]
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        float *r = red + (warp * G + g) * (kDh + 1);
-        f2_split(acc[g][0], r[4 * lane], r[4 * lane + 1]);
-        f2_split(acc[g][1], r[4 * lane + 2], r[4 * lane + 3]);
-        if (lane == 0) r[kDh] = l[g];
+        float lv = l[g];
+#pragma unroll
+        for (int off = 2; off <= 16; off <<= 1) lv += __shfl_xor_sync(WSW_FULL_MASK, lv, off);
+        float v8[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            f2_split(acc[g][k], v8[2 * k], v8[2 * k + 1]);
+            v8[2 * k] += __shfl_xor_sync(WSW_FULL_MASK, v8[2 * k], 16);
+            v8[2 * k + 1] += __shfl_xor_sync(WSW_FULL_MASK, v8[2 * k + 1], 16);
+        }
+        float *r = red + (warp * G + g) * kRed;
+        if (hf == 0) {
+            reinterpret_cast<float4 *>(r + 4 + 8 * c)[0] = make_float4(v8[0], v8[1], v8[2], v8[3]);
+            reinterpret_cast<float4 *>(r + 4 + 8 * c)[1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+        }
+        if (lane == 0) {
+            r[0] = m[g];
+            r[1] = lv;
+        }
     }
     __syncthreads();
     for (int i = tid; i < G * (kDh + 1); i += kThreads) {
         const int g = i / (kDh + 1), e = i - g * (kDh + 1);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int ww = 0; ww < kWWarps; ++ww) mx = fmaxf(mx, red[(ww * G + g) * kRed]);
         float sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) sum += red[(w * G + g) * (kDh + 1) + e];
+        for (int ww = 0; ww < kWWarps; ++ww) {
+            const float *r = red + (ww * G + g) * kRed;
+            const float f = r[0] == -INFINITY ? 0.f : exp2f(r[0] - mx);
+            sum = fmaf(e < kDh ? r[4 + e] : r[1], f, sum);
+        }
         float *dst = a.ws + ((static_cast<int64_t>(h) * a.splits + blockIdx.x) * G + g) * kPart;
         if (e < kDh) dst[2 + e] = sum;
         else {
-            dst[0] = mrun[g];
+            dst[0] = mx;
             dst[1] = sum;
         }
     }
 }
 
-// One CTA per (head, query) of 512 threads: the global maximum and the factor
-// exp2(m_s - m) of every chunk first, then four slices of 128 threads (one per
-// dimension) add the chunks s = slice, slice + 4, ... in order, and the slices are added
-// in a fixed order.  Many chunks' loads are in flight at once.
+// One CTA per (head, query) of 512 threads in four slices of 128 (one thread per
+// dimension).  A slice takes the chunks s = slice, slice + 4, ... in order, loading each
+// chunk's maximum, weight sum and value in one round and keeping a running maximum (the
+// sums so far are rescaled when it grows); the slices are then merged in a fixed order,
+// so the result does not depend on the launch.
 constexpr int kCombThreads = 4 * kDh;
 
 __global__ void __launch_bounds__(kCombThreads) attn_decode_combine_kernel(const AttnArgs a, int G) {
-    __shared__ float fac[kTargetCtas];  // splits <= kTargetCtas
-    __shared__ float wmax[kCombThreads / 32];
-    __shared__ float num_s[4][kDh], den_s[4];
+    __shared__ float m_s[4], num_s[4][kDh], den_s[4];
     const int hg = blockIdx.x;  // h * G + g
     const int h = hg / G, g = hg - h * G;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
+    const int sl = tid / kDh, d = tid % kDh;
+    // the next launch may take the SMs now: it reads nothing of this one before its own
+    // dependency wait
+    pdl_launch_dependents();
     pdl_wait();
     const float *part = a.ws + (static_cast<int64_t>(h) * a.splits * G + g) * kPart;
     const int64_t step = static_cast<int64_t>(G) * kPart;  // from one chunk to the next
-    float m = -INFINITY;
-    for (int s = tid; s < a.splits; s += kCombThreads) m = fmaxf(m, part[s * step]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(WSW_FULL_MASK, m, off));
-    if (lane == 0) wmax[warp] = m;
-    __syncthreads();
-    m = wmax[0];
-#pragma unroll
-    for (int w = 1; w < kCombThreads / 32; ++w) m = fmaxf(m, wmax[w]);
-    for (int s = tid; s < a.splits; s += kCombThreads) fac[s] = exp2f(part[s * step] - m);
-    __syncthreads();
-    const int sl = tid / kDh, d = tid % kDh;
-    float num = 0.f, den = 0.f;
-#pragma unroll 8
+    float m = -INFINITY, num = 0.f, den = 0.f;
+#pragma unroll 4
     for (int s = sl; s < a.splits; s += 4) {
         const float *ps = part + s * step;
-        num = fmaf(ps[2 + d], fac[s], num);
-        den = fmaf(ps[1], fac[s], den);
+        const float ms = ps[0], ls = ps[1], xs = ps[2 + d];
+        if (ms > m) {
+            const float f = m == -INFINITY ? 0.f : exp2f(m - ms);
+            num *= f;
+            den *= f;
+            m = ms;
+        }
+        const float f = ms == -INFINITY ? 0.f : exp2f(ms - m);
+        num = fmaf(xs, f, num);
+        den = fmaf(ls, f, den);
     }
     num_s[sl][d] = num;
-    if (d == 0) den_s[sl] = den;
+    if (d == 0) {
+        m_s[sl] = m;
+        den_s[sl] = den;
+    }
     __syncthreads();
-    pdl_launch_dependents();
     if (sl == 0) {
-        const float n = (num_s[0][d] + num_s[1][d]) + (num_s[2][d] + num_s[3][d]);
-        const float dn = (den_s[0] + den_s[1]) + (den_s[2] + den_s[3]);
+        const float mx = fmaxf(fmaxf(m_s[0], m_s[1]), fmaxf(m_s[2], m_s[3]));
+        float f[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f[i] = m_s[i] == -INFINITY ? 0.f : exp2f(m_s[i] - mx);
+        const float n = (num_s[0][d] * f[0] + num_s[1][d] * f[1]) + (num_s[2][d] * f[2] + num_s[3][d] * f[3]);
+        const float dn = (den_s[0] * f[0] + den_s[1] * f[1]) + (den_s[2] * f[2] + den_s[3] * f[3]);
         a.out[static_cast<int64_t>(hg) * kDh + d] = n / dn;
     }
 }
 
-// Positions per CTA and CTAs per head: about kTargetCtas CTAs over all heads, chunks a
-// whole number of tiles.
+// Positions per CTA and CTAs per head: about kWTargetCtas CTAs over all heads, chunks a
+// whole number of 16-position steps.
 void attn_split(int64_t depth, int64_t heads, int *chunk, int *splits) {
-    const int64_t want = kTargetCtas / heads > 1 ? kTargetCtas / heads : 1;
+    const int64_t want = kWTargetCtas / heads > 1 ? kWTargetCtas / heads : 1;
     int64_t c = (depth + want - 1) / want;
-    c = (c + kTile - 1) / kTile * kTile;
+    c = (c + kWBatch - 1) / kWBatch * kWBatch;
     *chunk = static_cast<int>(c);
     *splits = static_cast<int>((depth + c - 1) / c);
 }
 
 template <int G>
-cudaError_t launch_split(const AttnArgs &a, cudaStream_t s, bool pdl) {
-    const int smem = 2 * kStages * kTileBytes + (G * kDh + 2 * G * kTile + 2 * G) * 4;
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(attn_decode_split_kernel<G>), smem);
+cudaError_t launch_warp(const AttnArgs &a, cudaStream_t s, bool pdl) {
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(attn_decode_warp_kernel<G>), kWSmem);
     if (e != cudaSuccess) return e;
-    return launch(attn_decode_split_kernel<G>, dim3(a.splits, a.heads), dim3(kThreads), smem, s, pdl, a);
+    return launch(attn_decode_warp_kernel<G>, dim3(a.splits, a.heads), dim3(kThreads), kWSmem, s, pdl, a);
 }
 
 }  // namespace
@@ -400,10 +420,10 @@ extern "C" int wsw_attn_decode_f16(const float *q, const uint16_t *k, const uint
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (group) {
-        case 1: e = launch_split<1>(a, s, o.pdl); break;
-        case 2: e = launch_split<2>(a, s, o.pdl); break;
-        case 4: e = launch_split<4>(a, s, o.pdl); break;
-        default: e = launch_split<8>(a, s, o.pdl); break;
+        case 1: e = launch_warp<1>(a, s, o.pdl); break;
+        case 2: e = launch_warp<2>(a, s, o.pdl); break;
+        case 4: e = launch_warp<4>(a, s, o.pdl); break;
+        default: e = launch_warp<8>(a, s, o.pdl); break;
     }
     if (e != cudaSuccess) return WSW_ERR_CUDA;
     e = launch(attn_decode_combine_kernel, dim3(static_cast<unsigned>(heads * group)), dim3(kCombThreads), 0, s,
