@@ -508,7 +508,7 @@ def measure_attn_decode(torch, wsw, dev, out):
         for group in (1, 8):
             qq = torch.randn((4, group, 128), generator=g, device=dev)
             o = torch.empty((4, group, 128), dtype=torch.float32, device=dev)
-            ws = torch.empty(wsw.attn_decode_workspace_bytes(depth, 4, group), dtype=torch.uint8, device=dev)
+            ws = torch.zeros(wsw.attn_decode_workspace_bytes(depth, 4, group), dtype=torch.uint8, device=dev)
             for layout in ("per_head", "position_major"):
                 it = [0]
 

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define WSW_ABI_VERSION 6
+#define WSW_ABI_VERSION 7
 
 typedef enum wsw_status {
     WSW_OK = 0,
@@ -334,11 +334,15 @@ int wsw_dequant_q8_0_kv(const int8_t *q, const uint16_t *d, int64_t depth, int64
  *   k, v   binary16; 16-byte aligned, strides multiples of 8 elements.
  *   out    fp32 [heads][group][head_dim]; must not overlap the inputs.
  *   ws     device workspace of ws_bytes >= wsw_attn_decode_workspace_bytes(depth,
- *          heads, group) bytes, 16-byte aligned, overwritten (WSW_ERR_WORKSPACE
- *          otherwise).  Two calls in flight at once need two workspaces.
+ *          heads, group) bytes (WSW_ERR_WORKSPACE otherwise), 16-byte aligned.  It
+ *          starts with one arrival counter per head, which must be zero before the
+ *          first call; every call that completes leaves them zero, so a workspace is
+ *          zero-filled once and then reused.  The rest is overwritten.  Two calls in
+ *          flight at once need two workspaces.
  *   depth >= 1;  group in {1, 2, 4, 8};  head_dim == 128;  heads <= 65535
  *   (WSW_ERR_UNSUPPORTED otherwise).
- * Two launches: chunks of positions in parallel, then their combination (PDL-linked).
+ * One launch: chunks of positions in parallel; the last chunk of a head to finish
+ * merges that head's chunks.
  */
 size_t wsw_attn_decode_workspace_bytes(int64_t depth, int64_t heads, int64_t group);
 int wsw_attn_decode_f16(const float *q, const uint16_t *k, const uint16_t *v, int64_t depth,

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert wsw.abi_version() == 6
+    assert wsw.abi_version() == 7
     assert wsw.status_string(0) == "WSW_OK"
     assert wsw.status_string(1) == "WSW_ERR_INVALID_ARG"
     assert wsw.status_string(2) == "WSW_ERR_MISALIGNED"
@@ -118,11 +118,12 @@ def test_other_calls_reject_on_host(lib):
     assert c(-1, None, None, None) == INVALID
     assert c(0, None, None, None) == 0
     ab = lib.wsw_attn_decode_workspace_bytes
-    # one partial (max, sum, 128 values) per (chunk, head, query); chunks of whole
-    # 16-position steps, about 152 of them over all heads
-    assert ab(32768, 4, 8) == 38 * 4 * 8 * 130 * 4
-    assert ab(65536, 1, 1) == 152 * 130 * 4
-    assert ab(1, 4, 1) == 4 * 130 * 4
+    # one arrival counter per head (padded to 16 bytes), then one record (max, sum, two
+    # pad, 128 values) per (chunk, head, query); chunks of whole 16-position steps,
+    # about 152 of them over all heads
+    assert ab(32768, 4, 8) == 16 + 38 * 4 * 8 * 132 * 4
+    assert ab(65536, 1, 1) == 16 + 152 * 132 * 4
+    assert ab(1, 5, 1) == 32 + 5 * 132 * 4
     assert ab(0, 4, 1) == 0 and ab(64, 4, 16) == 0
     a = lib.wsw_attn_decode_f16
     A = P(4096)

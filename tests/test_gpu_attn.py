@@ -120,3 +120,26 @@ def test_dequant_then_attend(orc):
     kb, vb = orc.dequant_q8_0_kv(qk, dk), orc.dequant_q8_0_kv(qv, dv)
     ref = orc.attn_decode(q.numpy(), kb, vb, 1 / math.sqrt(hd))
     _check(got, ref, _magnitude(q.numpy(), kb, vb, 1 / math.sqrt(hd)), "dequant then attend")
+
+
+def test_workspace_reused_across_shapes_and_left_zeroed(orc):
+    """One zero-filled workspace serves calls of different shapes in turn: the last
+    chunk of each head merges, then sets its arrival counter back to zero, and repeated
+    calls give the same bits whichever CTA merged."""
+    wsw = need_gpu()
+    shapes = [(4, 1, 5000), (2, 8, 777), (1, 2, 64), (3, 4, 20000), (4, 1, 5000)]
+    ws = torch.zeros(max(wsw.attn_decode_workspace_bytes(d, h, g) for h, g, d in shapes), dtype=torch.uint8,
+                     device="cuda")
+    for heads, group, depth in shapes:
+        q, k, v = _inputs(6, heads, group, depth)
+        kb, vb = f16_bits(k), f16_bits(v)
+        ref = orc.attn_decode(q.numpy(), kb, vb, 0.1)
+        mag = _magnitude(q.numpy(), kb, vb, 0.1)
+        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+        first = wsw.attn_decode_f16(qd, kd, vd, scale=0.1, ws=ws)
+        _check(first, ref, mag, "shape %s" % ((heads, group, depth),))
+        for _ in range(3):
+            again = wsw.attn_decode_f16(qd, kd, vd, scale=0.1, ws=ws)
+            assert torch.equal(first.view(torch.int32), again.view(torch.int32))
+        torch.cuda.synchronize()
+        assert int(ws[:4 * heads].view(torch.int32).abs().sum()) == 0, "counters left nonzero"

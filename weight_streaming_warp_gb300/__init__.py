@@ -327,7 +327,8 @@ def attn_decode_f16(q, k, v, scale=None, out=None, ws=None, opts=None):
     position strides (the per-head-contiguous scratch as is, the position-major cache
     as cache.permute(1, 0, 2)).  scale defaults to 1/sqrt(head_dim).  Returns out fp32
     [heads][group][head_dim].  ws: a uint8 device tensor of at least
-    attn_decode_workspace_bytes(depth, heads, group) bytes, allocated if None."""
+    attn_decode_workspace_bytes(depth, heads, group) bytes, zero-filled before its first
+    use (every call leaves it ready for the next), allocated if None."""
     _dev(q, torch.float32, "q")
     _dev(k, torch.float16, "k")
     _dev(v, torch.float16, "v")
@@ -343,7 +344,7 @@ def attn_decode_f16(q, k, v, scale=None, out=None, ws=None, opts=None):
     y = out if out is not None else torch.empty((heads, group, hd), dtype=torch.float32, device=q.device)
     need = attn_decode_workspace_bytes(depth, heads, group)
     if ws is None:
-        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=q.device)
     _check(load().wsw_attn_decode_f16(q.data_ptr(), k.data_ptr(), v.data_ptr(), depth, heads, group, hd,
                                       k.stride(1), k.stride(0), v.stride(1), v.stride(0), float(scale),
                                       y.data_ptr(), ws.data_ptr(), ws.numel(), _stream(), _opts(opts)),

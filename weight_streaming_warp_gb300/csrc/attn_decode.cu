@@ -10,7 +10,7 @@
 //   s_p          = scale * q[h][g] . K(h, p)
 //   out[h][g][i] = sum_p exp(s_p - m) V(h, p)[i] / sum_p exp(s_p - m),  m = max_p s_p
 //
-// Design (GB300), flash decoding in two launches:
+// Design (GB300), flash decoding in one launch:
 //  * attn_decode_warp_kernel: grid (splits, heads) of about one CTA per SM, 256 threads.
 //    A CTA takes a chunk of positions of one KV head for all G query heads of its group,
 //    so every K and V byte is read once per step.  Each of its eight warps walks its own
@@ -19,11 +19,18 @@
 //    merged once at the end, and the CTA writes (m, l = sum of weights, acc[128]) of each
 //    query to the workspace.  Scores are kept in the log2 domain (scale * log2 e folded
 //    into q), so the weights are exp2f(s - m).
-//  * attn_decode_combine_kernel (PDL-linked): one CTA per (head, query); rescales every
-//    chunk's partials to a common maximum, adds them in a fixed order and divides, so
-//    the result does not depend on the launch.
-//  * The dot products and the value sums use packed fp32x2 FMAs (even and odd
-//    dimensions in the two lanes), which halves their instruction count.
+//  * The last CTA of a head to finish (an arrival counter per head in the workspace)
+//    rescales every chunk's record to the common maximum, adds them in a fixed order and
+//    divides, so the result does not depend on the launch; it then sets the counter back
+//    to zero.  A second launch for this merge measured 4-5 us slower per call: its
+//    dependency hop sat on the critical path.
+//  * Groups of one and two query heads run on the CUDA cores: the dot products and the
+//    value sums use packed fp32x2 FMAs (even and odd dimensions in the two lanes), and
+//    the loop is bound by memory.  Groups of four and eight run the two products of a
+//    step on the tensor cores (m16n8k16, fp32 accumulation): on the CUDA cores their
+//    loop was bound by instruction issue, 1.7x slower.  The fp32 queries and weights
+//    enter as a binary16 high part plus a binary16 residual, in the two halves of the
+//    16-row operand, so their products keep about 22 bits.
 // The split count is a function of (depth, heads) alone, never of the device or the
 // launch options.
 #include <cuda_fp16.h>
@@ -38,7 +45,7 @@ namespace {
 constexpr int kDh = 128;                // head_dim
 constexpr int kThreads = 256;           // 8 warps
 constexpr int kRowBytes = kDh * 2;      // one K or V row in shared memory
-constexpr int kPart = kDh + 2;          // floats per (chunk, head, query): m, l, acc
+constexpr int kPart = kDh + 4;          // floats per (chunk, head, query): m, l, 2 pad, acc
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnArgs {
@@ -49,7 +56,8 @@ struct AttnArgs {
     int chunk;                          // positions per CTA (whole 16-position steps)
     int splits;
     int heads;
-    float *ws;
+    unsigned *cnt;                      // [heads] arrival counters (zero between calls)
+    float *part;                        // [heads][splits][G][kPart] partial records
     float *out;
 };
 
@@ -92,7 +100,7 @@ __device__ __forceinline__ uint64_t h2_to_f2(uint32_t h) {
 //   softmax: the step's maximum over the warp, then each lane's weight exp2(s - m)
 //   values:  each row's weight is shuffled from the lane that holds it
 // At the end the warps' partials are merged once in shared memory (one barrier) and the
-// CTA writes the same (m, l, acc) record as the tile form, for the same combine launch.
+// CTA writes its (m, l, acc) record; the last CTA of the head merges the records.
 constexpr int kWBatch = 16;                                // positions per warp step
 constexpr int kWStages = 3;
 constexpr int kWWarps = kThreads / 32;
@@ -100,6 +108,27 @@ constexpr int kWStageBytes = 2 * kWBatch * kRowBytes;       // K and V rows of o
 constexpr int kWSmem = kWWarps * kWStages * kWStageBytes;   // 192 KB: one CTA per SM
 constexpr int kWTargetCtas = 152;                          // one CTA per SM of a 152-SM part
 constexpr int kRed = kDh + 4;  // floats per warp partial in the merge: m, l, 2 pad, acc (16-byte aligned)
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 x) { return *reinterpret_cast<uint32_t *>(&x); }
+// D += A B for one m16n8k16 tile: binary16 operands, fp32 accumulation
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p)))
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p)))
+                 : "memory");
+}
 
 // 16-byte copy that writes zeros and reads nothing when !valid (src must still be mapped)
 __device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid) {
@@ -109,7 +138,64 @@ __device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, boo
                  : "memory");
 }
 
+// The merge of one head's chunks, by the last CTA to finish.  Thread (slice, query,
+// 16-byte column) takes the chunks s = slice, slice + 8 / G, ... in order, loading each
+// chunk's maximum, weight sum and four values in one round and keeping a running
+// maximum (what it has added so far is rescaled when the maximum grows); the 8 / G
+// slices are then merged in a fixed order.  The result depends on neither the CTA that
+// merges nor the launch.  sm: 1024 + 16 G floats of shared memory.
 template <int G>
+__device__ __forceinline__ void merge_chunks(const AttnArgs &a, int h, float *sm) {
+    constexpr int kSl = kWWarps / G;  // slices of the chunk list
+    const int tid = threadIdx.x;
+    const int S = a.splits;
+    float *sums = sm;                          // [kSl][G][kDh]
+    float *msl = sums + kSl * G * kDh;         // [kSl][G]
+    float *lsl = msl + kSl * G;                // [kSl][G]
+    const float *part = a.part + static_cast<int64_t>(h) * S * G * kPart;  // [S][G][kPart]
+    const int sl = tid / (G * 32), gq = tid - sl * (G * 32);
+    const int g = gq >> 5, c4 = gq & 31;  // query, 16-byte column (dimensions 4 c4 .. 4 c4 + 3)
+    float m = -INFINITY, l = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int sidx = sl; sidx < S; sidx += kSl) {
+        const float *r = part + (static_cast<int64_t>(sidx) * G + g) * kPart;
+        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(r));
+        const float4 x = __ldcg(reinterpret_cast<const float4 *>(r + 4) + c4);
+        const float mn = fmaxf(m, ml.x);
+        const float fo = m == -INFINITY ? 0.f : exp2f(m - mn);     // rescales what was added
+        const float fn = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mn);
+        m = mn;
+        l = l * fo + ml.y * fn;
+        acc.x = acc.x * fo + x.x * fn;
+        acc.y = acc.y * fo + x.y * fn;
+        acc.z = acc.z * fo + x.z * fn;
+        acc.w = acc.w * fo + x.w * fn;
+    }
+    reinterpret_cast<float4 *>(sums + (sl * G + g) * kDh)[c4] = acc;
+    if (c4 == 0) {
+        msl[sl * G + g] = m;
+        lsl[sl * G + g] = l;
+    }
+    __syncthreads();
+    for (int i = tid; i < G * kDh; i += kThreads) {
+        const int gg = i / kDh;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kSl; ++k) mx = fmaxf(mx, msl[k * G + gg]);
+        float n = 0.f, dn = 0.f;
+#pragma unroll
+        for (int k = 0; k < kSl; ++k) {
+            const float ms = msl[k * G + gg];
+            const float f = ms == -INFINITY ? 0.f : exp2f(ms - mx);
+            n = fmaf(sums[k * G * kDh + i], f, n);
+            dn = fmaf(lsl[k * G + gg], f, dn);
+        }
+        a.out[static_cast<int64_t>(h) * G * kDh + i] = n / dn;
+    }
+}
+
+template <int G, bool TC>
 __global__ void __launch_bounds__(kThreads, 1) attn_decode_warp_kernel(const AttnArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -143,8 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_warp_kernel(const Att
                 const int r = 2 * i + hf;
                 const bool ok = pb + r < w1;
                 const int64_t p = ok ? pb + r : w0;
-                cp_async16_zfill(stg + r * kRowBytes + c * 16, kh + p * a.kps + c * 8, ok);
-                cp_async16_zfill(stg + (kWBatch + r) * kRowBytes + c * 16, vh + p * a.vps + c * 8, ok);
+                const int sw = (c ^ (r & 7)) * 16;  // piece c of row r, XOR-swizzled
+                cp_async16_zfill(stg + r * kRowBytes + sw, kh + p * a.kps + c * 8, ok);
+                cp_async16_zfill(stg + (kWBatch + r) * kRowBytes + sw, vh + p * a.vps + c * 8, ok);
             }
             if (++ist == kWStages) ist = 0;
         }
@@ -153,131 +240,251 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_warp_kernel(const Att
     issue(0);
     issue(1);
 
-    // this lane's eight dimensions of every query, in the log2 domain
-    uint64_t qv[G][4];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float *qp = a.q + (static_cast<int64_t>(h) * G + g) * kDh + c * 8;  // 4-byte aligned
-#pragma unroll
-        for (int k = 0; k < 4; ++k) qv[g][k] = f2(qp[2 * k] * a.qscale, qp[2 * k + 1] * a.qscale);
-    }
-    pdl_launch_dependents();
-
-    float m[G], l[G];
-    uint64_t acc[G][4];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = -INFINITY;
-        l[g] = 0.f;
-        acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0ull;
-    }
-    const bool b3 = c & 8, b2 = c & 4, b1 = c & 2;
-    const int row = 2 * (c >> 1) + hf;  // the row whose score this lane ends with
-
-    int rst = 0;  // ring stage of the step being used
-    for (int t = 0; t < nsteps; ++t) {
-        issue(t + 2);
-        cp_async_wait<2>();
-        const unsigned char *stg = ring + rst * kWStageBytes;
-        if (++rst == kWStages) rst = 0;
-        const bool valid = w0 + static_cast<int64_t>(t) * kWBatch + row < w1;
-
-        uint64_t kf[kWBatch / 2][4];
-#pragma unroll
-        for (int i = 0; i < kWBatch / 2; ++i) {
-            const uint4 kv = *reinterpret_cast<const uint4 *>(stg + (2 * i + hf) * kRowBytes + c * 16);
-            kf[i][0] = h2_to_f2(kv.x);
-            kf[i][1] = h2_to_f2(kv.y);
-            kf[i][2] = h2_to_f2(kv.z);
-            kf[i][3] = h2_to_f2(kv.w);
-        }
-        float w[G];
-#pragma unroll
+    float *red = reinterpret_cast<float *>(smem);  // the warps' partials [8][G][kRed], after the loop
+    if constexpr (!TC) {
+        // this lane's eight dimensions of every query, in the log2 domain
+        uint64_t qv[G][4];
+    #pragma unroll
         for (int g = 0; g < G; ++g) {
-            float d[kWBatch / 2];
-#pragma unroll
-            for (int i = 0; i < kWBatch / 2; ++i) {
-                uint64_t x = 0ull;
-                fma2(x, qv[g][0], kf[i][0]);
-                fma2(x, qv[g][1], kf[i][1]);
-                fma2(x, qv[g][2], kf[i][2]);
-                fma2(x, qv[g][3], kf[i][3]);
-                d[i] = f2_sum(x);
-            }
-            // butterfly over the half-warp: after the shuffle at distance 8 a lane keeps
-            // rows 0..3 or 4..7 (by bit 3 of c), at 4 two of those, at 2 one, and the
-            // shuffle at 1 completes the sum
-            float e4[4], e2[2];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float send = b3 ? d[k] : d[k + 4], keep = b3 ? d[k + 4] : d[k];
-                e4[k] = keep + __shfl_xor_sync(WSW_FULL_MASK, send, 8);
-            }
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const float send = b2 ? e4[k] : e4[k + 2], keep = b2 ? e4[k + 2] : e4[k];
-                e2[k] = keep + __shfl_xor_sync(WSW_FULL_MASK, send, 4);
-            }
-            const float send = b1 ? e2[0] : e2[1], keep = b1 ? e2[1] : e2[0];
-            const float e1 = keep + __shfl_xor_sync(WSW_FULL_MASK, send, 2);
-            float s = e1 + __shfl_xor_sync(WSW_FULL_MASK, e1, 1);
-            if (!valid) s = -INFINITY;
-            // online softmax: the step's maximum over the warp (lane pairs hold equal scores)
-            float mt = s;
-#pragma unroll
-            for (int off = 2; off <= 16; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(WSW_FULL_MASK, mt, off));
-            const float mn = fmaxf(m[g], mt);
-            const bool none = mn == -INFINITY;
-            const float al = none ? 1.f : exp2f(m[g] - mn);
-            w[g] = none ? 0.f : exp2f(s - mn);
-            m[g] = mn;
-            l[g] = l[g] * al + w[g];
-            const uint64_t al2 = f2(al, al);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(acc[g][k]) : "l"(al2));
+            const float *qp = a.q + (static_cast<int64_t>(h) * G + g) * kDh + c * 8;  // 4-byte aligned
+    #pragma unroll
+            for (int k = 0; k < 4; ++k) qv[g][k] = f2(qp[2 * k] * a.qscale, qp[2 * k + 1] * a.qscale);
         }
-        // values: row 2 i + hf, piece c; its weight sits in lane 16 hf + 2 i
-#pragma unroll
-        for (int i = 0; i < kWBatch / 2; ++i) {
-            const uint4 vv = *reinterpret_cast<const uint4 *>(stg + (kWBatch + 2 * i + hf) * kRowBytes + c * 16);
-            const uint64_t v01 = h2_to_f2(vv.x), v23 = h2_to_f2(vv.y), v45 = h2_to_f2(vv.z), v67 = h2_to_f2(vv.w);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float wi = __shfl_sync(WSW_FULL_MASK, w[g], (lane & 16) | (2 * i));
-                const uint64_t w2 = f2(wi, wi);
-                fma2(acc[g][0], w2, v01);
-                fma2(acc[g][1], w2, v23);
-                fma2(acc[g][2], w2, v45);
-                fma2(acc[g][3], w2, v67);
-            }
-        }
-    }
-    cp_async_wait<0>();
+        pdl_launch_dependents();
 
-    // the warp's partial: the two half-warps' value sums added, the weight sum over the
-    // lanes of one parity of each pair (pairs hold equal weights)
-    __syncthreads();  // every warp is past its ring: it becomes the merge area
-    float *red = reinterpret_cast<float *>(smem);  // [8 warps][G][kRed]
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        float lv = l[g];
-#pragma unroll
-        for (int off = 2; off <= 16; off <<= 1) lv += __shfl_xor_sync(WSW_FULL_MASK, lv, off);
-        float v8[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            f2_split(acc[g][k], v8[2 * k], v8[2 * k + 1]);
-            v8[2 * k] += __shfl_xor_sync(WSW_FULL_MASK, v8[2 * k], 16);
-            v8[2 * k + 1] += __shfl_xor_sync(WSW_FULL_MASK, v8[2 * k + 1], 16);
+        float m[G], l[G];
+        uint64_t acc[G][4];
+    #pragma unroll
+        for (int g = 0; g < G; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+            acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0ull;
         }
-        float *r = red + (warp * G + g) * kRed;
-        if (hf == 0) {
-            reinterpret_cast<float4 *>(r + 4 + 8 * c)[0] = make_float4(v8[0], v8[1], v8[2], v8[3]);
-            reinterpret_cast<float4 *>(r + 4 + 8 * c)[1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+        const bool b3 = c & 8, b2 = c & 4, b1 = c & 2;
+        const int row = 2 * (c >> 1) + hf;  // the row whose score this lane ends with
+
+        int rst = 0;  // ring stage of the step being used
+        for (int t = 0; t < nsteps; ++t) {
+            issue(t + 2);
+            cp_async_wait<2>();
+            const unsigned char *stg = ring + rst * kWStageBytes;
+            if (++rst == kWStages) rst = 0;
+            const bool valid = w0 + static_cast<int64_t>(t) * kWBatch + row < w1;
+
+            uint64_t kf[kWBatch / 2][4];
+    #pragma unroll
+            for (int i = 0; i < kWBatch / 2; ++i) {
+                const int r = 2 * i + hf;
+                const uint4 kv = *reinterpret_cast<const uint4 *>(stg + r * kRowBytes + ((c ^ (r & 7)) << 4));
+                kf[i][0] = h2_to_f2(kv.x);
+                kf[i][1] = h2_to_f2(kv.y);
+                kf[i][2] = h2_to_f2(kv.z);
+                kf[i][3] = h2_to_f2(kv.w);
+            }
+            float w[G];
+    #pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float d[kWBatch / 2];
+    #pragma unroll
+                for (int i = 0; i < kWBatch / 2; ++i) {
+                    uint64_t x = 0ull;
+                    fma2(x, qv[g][0], kf[i][0]);
+                    fma2(x, qv[g][1], kf[i][1]);
+                    fma2(x, qv[g][2], kf[i][2]);
+                    fma2(x, qv[g][3], kf[i][3]);
+                    d[i] = f2_sum(x);
+                }
+                // butterfly over the half-warp: after the shuffle at distance 8 a lane keeps
+                // rows 0..3 or 4..7 (by bit 3 of c), at 4 two of those, at 2 one, and the
+                // shuffle at 1 completes the sum
+                float e4[4], e2[2];
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float send = b3 ? d[k] : d[k + 4], keep = b3 ? d[k + 4] : d[k];
+                    e4[k] = keep + __shfl_xor_sync(WSW_FULL_MASK, send, 8);
+                }
+    #pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float send = b2 ? e4[k] : e4[k + 2], keep = b2 ? e4[k + 2] : e4[k];
+                    e2[k] = keep + __shfl_xor_sync(WSW_FULL_MASK, send, 4);
+                }
+                const float send = b1 ? e2[0] : e2[1], keep = b1 ? e2[1] : e2[0];
+                const float e1 = keep + __shfl_xor_sync(WSW_FULL_MASK, send, 2);
+                float s = e1 + __shfl_xor_sync(WSW_FULL_MASK, e1, 1);
+                if (!valid) s = -INFINITY;
+                // online softmax: the step's maximum over the warp (lane pairs hold equal scores)
+                float mt = s;
+    #pragma unroll
+                for (int off = 2; off <= 16; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(WSW_FULL_MASK, mt, off));
+                const float mn = fmaxf(m[g], mt);
+                const bool none = mn == -INFINITY;
+                const float al = none ? 1.f : exp2f(m[g] - mn);
+                w[g] = none ? 0.f : exp2f(s - mn);
+                m[g] = mn;
+                l[g] = l[g] * al + w[g];
+                const uint64_t al2 = f2(al, al);
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(acc[g][k]) : "l"(al2));
+            }
+            // values: row 2 i + hf, piece c; its weight sits in lane 16 hf + 2 i
+    #pragma unroll
+            for (int i = 0; i < kWBatch / 2; ++i) {
+                const int r = 2 * i + hf;
+                const uint4 vv = *reinterpret_cast<const uint4 *>(stg + (kWBatch + r) * kRowBytes + ((c ^ (r & 7)) << 4));
+                const uint64_t v01 = h2_to_f2(vv.x), v23 = h2_to_f2(vv.y), v45 = h2_to_f2(vv.z), v67 = h2_to_f2(vv.w);
+    #pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float wi = __shfl_sync(WSW_FULL_MASK, w[g], (lane & 16) | (2 * i));
+                    const uint64_t w2 = f2(wi, wi);
+                    fma2(acc[g][0], w2, v01);
+                    fma2(acc[g][1], w2, v23);
+                    fma2(acc[g][2], w2, v45);
+                    fma2(acc[g][3], w2, v67);
+                }
+            }
         }
-        if (lane == 0) {
-            r[0] = m[g];
-            r[1] = lv;
+        cp_async_wait<0>();
+
+        // the warp's partial: the two half-warps' value sums added, the weight sum over the
+        // lanes of one parity of each pair (pairs hold equal weights)
+        __syncthreads();  // every warp is past its ring: it becomes the merge area
+    #pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float lv = l[g];
+    #pragma unroll
+            for (int off = 2; off <= 16; off <<= 1) lv += __shfl_xor_sync(WSW_FULL_MASK, lv, off);
+            float v8[8];
+    #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                f2_split(acc[g][k], v8[2 * k], v8[2 * k + 1]);
+                v8[2 * k] += __shfl_xor_sync(WSW_FULL_MASK, v8[2 * k], 16);
+                v8[2 * k + 1] += __shfl_xor_sync(WSW_FULL_MASK, v8[2 * k + 1], 16);
+            }
+            float *r = red + (warp * G + g) * kRed;
+            if (hf == 0) {
+                reinterpret_cast<float4 *>(r + 4 + 8 * c)[0] = make_float4(v8[0], v8[1], v8[2], v8[3]);
+                reinterpret_cast<float4 *>(r + 4 + 8 * c)[1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+            }
+            if (lane == 0) {
+                r[0] = m[g];
+                r[1] = lv;
+            }
+        }
+    } else {
+        // Tensor-core form (m16n8k16, fp32 accumulation).  A holds 16 rows: the binary16
+        // high parts of the G queries in rows 0..7 and their residuals q - hi in rows
+        // 8..15 (rows past G are zero), so row g plus row g + 8 of a product is the fp32
+        // query's product to about 2^-22.  Scores: S = [q_hi; q_lo] K^T over 8 k-steps of
+        // 16 dimensions, two 8-position column blocks; the weights P take the same
+        // high / residual split as the A operand of O += [P_hi; P_lo] V.  K and V come
+        // from the swizzled ring by ldmatrix (V transposed).  Thread (group gq = lane / 4,
+        // tq = lane % 4) owns query gq and positions 8 n + 2 tq + {0, 1} of each block.
+        const int gq = lane >> 2, tq = lane & 3;
+        uint32_t qa[kDh / 16][4];
+#pragma unroll
+        for (int kt = 0; kt < kDh / 16; ++kt) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float x0 = 0.f, x1 = 0.f;
+                if (gq < G) {
+                    const float *qp = a.q + (static_cast<int64_t>(h) * G + gq) * kDh + 16 * kt + 8 * half + 2 * tq;
+                    x0 = qp[0] * a.qscale;
+                    x1 = qp[1] * a.qscale;
+                }
+                const __half2 hi = __floats2half2_rn(x0, x1);
+                const __half2 lo = __floats2half2_rn(x0 - __low2float(hi), x1 - __high2float(hi));
+                qa[kt][2 * half] = h2_bits(hi);
+                qa[kt][2 * half + 1] = h2_bits(lo);
+            }
+        }
+        pdl_launch_dependents();
+
+        float m = -INFINITY, l = 0.f;
+        float o[kDh / 8][4];
+#pragma unroll
+        for (int n = 0; n < kDh / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        // ldmatrix row addresses: lane L points at row L % 8 of matrix L / 8
+        const int mi = lane >> 3, mr = lane & 7;
+        const int kpos = 8 * (mi >> 1) + mr, kchunk = mi & 1;  // K: (block, k-half) per matrix
+        const int vpos = 8 * (mi & 1) + mr, vnt = mi >> 1;     // V: (position half, dims) per matrix
+
+        int rst = 0;
+        for (int t = 0; t < nsteps; ++t) {
+            __syncwarp();  // every lane is done reading the stage that step t + 2 reuses
+            issue(t + 2);
+            cp_async_wait<2>();
+            __syncwarp();  // the step's pieces copied by every lane are visible
+            const unsigned char *stg = ring + rst * kWStageBytes;
+            if (++rst == kWStages) rst = 0;
+            const int64_t pb = w0 + static_cast<int64_t>(t) * kWBatch;
+
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kt = 0; kt < kDh / 16; ++kt) {
+                uint32_t b[4];
+                const int ch = 2 * kt + kchunk;
+                ldsm_x4(b, stg + kpos * kRowBytes + ((ch ^ (kpos & 7)) << 4));
+                mma16816(sc[0], qa[kt], b[0], b[1]);
+                mma16816(sc[1], qa[kt], b[2], b[3]);
+            }
+            float sv[4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const bool ok = pb + 8 * n + 2 * tq + j < w1;
+                    sv[2 * n + j] = ok ? sc[n][j] + sc[n][2 + j] : -INFINITY;
+                }
+            float mt = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+            mt = fmaxf(mt, __shfl_xor_sync(WSW_FULL_MASK, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(WSW_FULL_MASK, mt, 2));
+            const float mn = fmaxf(m, mt);
+            const bool none = mn == -INFINITY;
+            const float al = none ? 1.f : exp2f(m - mn);
+            float p[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) p[i] = none ? 0.f : exp2f(sv[i] - mn);
+            m = mn;
+            l = l * al + ((p[0] + p[1]) + (p[2] + p[3]));
+            if (__any_sync(WSW_FULL_MASK, al != 1.f)) {
+#pragma unroll
+                for (int n = 0; n < kDh / 8; ++n) {
+                    o[n][0] *= al;
+                    o[n][1] *= al;
+                    o[n][2] *= al;
+                    o[n][3] *= al;
+                }
+            }
+            uint32_t pa[4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const __half2 hi = __floats2half2_rn(p[2 * n], p[2 * n + 1]);
+                const __half2 lo = __floats2half2_rn(p[2 * n] - __low2float(hi), p[2 * n + 1] - __high2float(hi));
+                pa[2 * n] = h2_bits(hi);
+                pa[2 * n + 1] = h2_bits(lo);
+            }
+#pragma unroll
+            for (int j = 0; j < kDh / 16; ++j) {
+                uint32_t b[4];
+                const int ch = 2 * j + vnt;
+                ldsm_x4_trans(b, stg + (kWBatch + vpos) * kRowBytes + ((ch ^ (vpos & 7)) << 4));
+                mma16816(o[2 * j], pa, b[0], b[1]);
+                mma16816(o[2 * j + 1], pa, b[2], b[3]);
+            }
+        }
+        cp_async_wait<0>();
+        __syncthreads();  // every warp is past its ring: it becomes the merge area
+        l += __shfl_xor_sync(WSW_FULL_MASK, l, 1);
+        l += __shfl_xor_sync(WSW_FULL_MASK, l, 2);
+        if (gq < G) {
+            float *r = red + (warp * G + gq) * kRed;
+#pragma unroll
+            for (int n = 0; n < kDh / 8; ++n)
+                *reinterpret_cast<float2 *>(r + 4 + 8 * n + 2 * tq) = make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
+            if (tq == 0) {
+                r[0] = m;
+                r[1] = l;
+            }
         }
     }
     __syncthreads();
@@ -293,65 +500,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_warp_kernel(const Att
             const float f = r[0] == -INFINITY ? 0.f : exp2f(r[0] - mx);
             sum = fmaf(e < kDh ? r[4 + e] : r[1], f, sum);
         }
-        float *dst = a.ws + ((static_cast<int64_t>(h) * a.splits + blockIdx.x) * G + g) * kPart;
-        if (e < kDh) dst[2 + e] = sum;
+        float *dst = a.part + ((static_cast<int64_t>(h) * a.splits + blockIdx.x) * G + g) * kPart;
+        if (e < kDh) dst[4 + e] = sum;
         else {
             dst[0] = mx;
             dst[1] = sum;
         }
     }
-}
 
-// One CTA per (head, query) of 512 threads in four slices of 128 (one thread per
-// dimension).  A slice takes the chunks s = slice, slice + 4, ... in order, loading each
-// chunk's maximum, weight sum and value in one round and keeping a running maximum (the
-// sums so far are rescaled when it grows); the slices are then merged in a fixed order,
-// so the result does not depend on the launch.
-constexpr int kCombThreads = 4 * kDh;
-
-__global__ void __launch_bounds__(kCombThreads) attn_decode_combine_kernel(const AttnArgs a, int G) {
-    __shared__ float m_s[4], num_s[4][kDh], den_s[4];
-    const int hg = blockIdx.x;  // h * G + g
-    const int h = hg / G, g = hg - h * G;
-    const int tid = threadIdx.x;
-    const int sl = tid / kDh, d = tid % kDh;
-    // the next launch may take the SMs now: it reads nothing of this one before its own
-    // dependency wait
-    pdl_launch_dependents();
-    pdl_wait();
-    const float *part = a.ws + (static_cast<int64_t>(h) * a.splits * G + g) * kPart;
-    const int64_t step = static_cast<int64_t>(G) * kPart;  // from one chunk to the next
-    float m = -INFINITY, num = 0.f, den = 0.f;
-#pragma unroll 4
-    for (int s = sl; s < a.splits; s += 4) {
-        const float *ps = part + s * step;
-        const float ms = ps[0], ls = ps[1], xs = ps[2 + d];
-        if (ms > m) {
-            const float f = m == -INFINITY ? 0.f : exp2f(m - ms);
-            num *= f;
-            den *= f;
-            m = ms;
-        }
-        const float f = ms == -INFINITY ? 0.f : exp2f(ms - m);
-        num = fmaf(xs, f, num);
-        den = fmaf(ls, f, den);
-    }
-    num_s[sl][d] = num;
-    if (d == 0) {
-        m_s[sl] = m;
-        den_s[sl] = den;
+    // The last CTA of the head to arrive merges every chunk's record.  The block barrier
+    // orders the CTA's record writes before thread 0's arrival, whose release (cumulative)
+    // publishes them at GPU scope; its acquire, and the barrier after it, order the
+    // merge's reads after every other CTA's arrival.
+    __shared__ int last;
+    __syncthreads();
+    if (tid == 0) {
+        unsigned old;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.cnt + h) : "memory");
+        last = old == static_cast<unsigned>(a.splits - 1);
     }
     __syncthreads();
-    if (sl == 0) {
-        const float mx = fmaxf(fmaxf(m_s[0], m_s[1]), fmaxf(m_s[2], m_s[3]));
-        float f[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) f[i] = m_s[i] == -INFINITY ? 0.f : exp2f(m_s[i] - mx);
-        const float n = (num_s[0][d] * f[0] + num_s[1][d] * f[1]) + (num_s[2][d] * f[2] + num_s[3][d] * f[3]);
-        const float dn = (den_s[0] * f[0] + den_s[1] * f[1]) + (den_s[2] * f[2] + den_s[3] * f[3]);
-        a.out[static_cast<int64_t>(hg) * kDh + d] = n / dn;
-    }
+    if (!last) return;
+    merge_chunks<G>(a, h, reinterpret_cast<float *>(smem));
+    if (tid == 0) a.cnt[h] = 0u;  // ready for the next call
 }
+
+// The workspace: one arrival counter per head (padded to 16 bytes), then the records.
+size_t counter_bytes(int64_t heads) { return static_cast<size_t>((heads * 4 + 15) / 16 * 16); }
 
 // Positions per CTA and CTAs per head: about kWTargetCtas CTAs over all heads, chunks a
 // whole number of 16-position steps.
@@ -363,11 +538,14 @@ void attn_split(int64_t depth, int64_t heads, int *chunk, int *splits) {
     *splits = static_cast<int>((depth + c - 1) / c);
 }
 
+// groups of four and eight query heads take the tensor-core form, smaller ones the
+// CUDA-core form (there the loop is bound by memory, not by issue)
 template <int G>
 cudaError_t launch_warp(const AttnArgs &a, cudaStream_t s, bool pdl) {
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(attn_decode_warp_kernel<G>), kWSmem);
+    constexpr bool tc = G >= 4;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(attn_decode_warp_kernel<G, tc>), kWSmem);
     if (e != cudaSuccess) return e;
-    return launch(attn_decode_warp_kernel<G>, dim3(a.splits, a.heads), dim3(kThreads), kWSmem, s, pdl, a);
+    return launch(attn_decode_warp_kernel<G, tc>, dim3(a.splits, a.heads), dim3(kThreads), kWSmem, s, pdl, a);
 }
 
 }  // namespace
@@ -379,7 +557,7 @@ extern "C" size_t wsw_attn_decode_workspace_bytes(int64_t depth, int64_t heads, 
         return 0;
     int chunk, splits;
     attn_split(depth, heads, &chunk, &splits);
-    return static_cast<size_t>(splits) * heads * group * kPart * sizeof(float);
+    return counter_bytes(heads) + static_cast<size_t>(splits) * heads * group * kPart * sizeof(float);
 }
 
 extern "C" int wsw_attn_decode_f16(const float *q, const uint16_t *k, const uint16_t *v, int64_t depth,
@@ -415,7 +593,8 @@ extern "C" int wsw_attn_decode_f16(const float *q, const uint16_t *k, const uint
     a.qscale = scale * kLog2e;
     attn_split(depth, heads, &a.chunk, &a.splits);
     a.heads = static_cast<int>(heads);
-    a.ws = static_cast<float *>(ws);
+    a.cnt = static_cast<unsigned *>(ws);
+    a.part = reinterpret_cast<float *>(static_cast<unsigned char *>(ws) + counter_bytes(heads));
     a.out = out;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -425,8 +604,5 @@ extern "C" int wsw_attn_decode_f16(const float *q, const uint16_t *k, const uint
         case 4: e = launch_warp<4>(a, s, o.pdl); break;
         default: e = launch_warp<8>(a, s, o.pdl); break;
     }
-    if (e != cudaSuccess) return WSW_ERR_CUDA;
-    e = launch(attn_decode_combine_kernel, dim3(static_cast<unsigned>(heads * group)), dim3(kCombThreads), 0, s,
-               true, a, static_cast<int>(group));
     return e == cudaSuccess ? WSW_OK : WSW_ERR_CUDA;
 }
