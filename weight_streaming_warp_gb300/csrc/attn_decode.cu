@@ -157,7 +157,10 @@ __device__ __forceinline__ void merge_chunks(const AttnArgs &a, int h, float *sm
     const int g = gq >> 5, c4 = gq & 31;  // query, 16-byte column (dimensions 4 c4 .. 4 c4 + 3)
     float m = -INFINITY, l = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
+    // deeper for the large groups, whose threads walk 8 / kSl times more records (the
+    // small groups measured slower with it: their main loop is larger)
+    constexpr int kUnroll = G >= 4 ? 16 : 8;
+#pragma unroll kUnroll
     for (int sidx = sl; sidx < S; sidx += kSl) {
         const float *r = part + (static_cast<int64_t>(sidx) * G + g) * kPart;
         const float2 ml = __ldcg(reinterpret_cast<const float2 *>(r));
