@@ -90,9 +90,13 @@ __device__ __forceinline__ uint64_t h2_to_f2(uint32_t h) {
 // Warp-streaming form: each of the eight warps walks its own run of whole 16-position
 // steps of the CTA's chunk through a private three-stage cp.async ring (8 KB a stage:
 // 16 K rows, then 16 V rows), and keeps its own running maximum, weight sum and value
-// sums; the loop has no block barrier.  A lane copies, and later reads, only its own
-// 16-byte pieces: half-warp hf holds rows hf, hf + 2, ..., piece c = lane % 16 of each
-// row (dimensions 8 c .. 8 c + 7), so no lane waits on another lane's copies.
+// sums; the loop has no block barrier.  Lane (hf = lane / 16, c = lane % 16) copies
+// piece c (dimensions 8 c .. 8 c + 7) of rows hf, hf + 2, ...; a row's 16-byte pieces
+// sit XOR-swizzled (piece c of row r in slot c ^ (r mod 8)), so that eight rows' equal
+// pieces fall in distinct banks.  The CUDA-core form below reads only the lane's own
+// pieces, so no lane waits on another's copies; the tensor-core form reads the stage
+// by ldmatrix after a warp barrier.
+// CUDA-core form:
 //   scores:  the lane's partial dots with its eight rows, summed over the half-warp by a
 //            butterfly that halves the values in flight at each of its four shuffles
 //            (8 shuffles for 8 rows); lanes 2 i and 2 i + 1 of half hf end with the
@@ -143,7 +147,7 @@ __device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, boo
 // chunk's maximum, weight sum and four values in one round and keeping a running
 // maximum (what it has added so far is rescaled when the maximum grows); the 8 / G
 // slices are then merged in a fixed order.  The result depends on neither the CTA that
-// merges nor the launch.  sm: 1024 + 16 G floats of shared memory.
+// merges nor the launch.  sm: 1040 floats of shared memory (kSl G = 8).
 template <int G>
 __device__ __forceinline__ void merge_chunks(const AttnArgs &a, int h, float *sm) {
     constexpr int kSl = kWWarps / G;  // slices of the chunk list
