@@ -171,6 +171,31 @@ def test_other_calls_reject_on_host(lib):
     assert b(1, P(4098), None) == MISALIGNED
 
 
+def test_attn_decode_workspace_covers_every_chunk(lib):
+    """Host planning of the decode attention: the workspace is the 16-byte padded
+    counter area plus one 132-float record per (chunk, head, query); the chunks are whole
+    16-position steps that cover the depth exactly (the last one non-empty), and there
+    are about one per SM over all heads (at most 152 per head, at most 152 in total once
+    the heads leave more than one chunk each)."""
+    ab = lib.wsw_attn_decode_workspace_bytes
+    for heads in (1, 2, 3, 4, 7, 8, 32, 64, 151, 152, 153, 1000):
+        for group in (1, 2, 4, 8):
+            for depth in (1, 15, 16, 17, 100, 999, 4096, 32768, 65537, 1 << 20):
+                n = ab(depth, heads, group)
+                counters = (heads * 4 + 15) // 16 * 16
+                rec = heads * group * 132 * 4
+                assert n > counters and (n - counters) % rec == 0, (depth, heads, group)
+                splits = (n - counters) // rec
+                want = max(152 // heads, 1)
+                assert 1 <= splits <= min(want, depth), (depth, heads, group, splits)
+                if heads <= 152:
+                    assert splits * heads <= 152
+                # some whole-step chunk size makes exactly `splits` chunks of the depth
+                chunk = -(-depth // want)
+                chunk = -(-chunk // 16) * 16
+                assert chunk % 16 == 0 and (splits - 1) * chunk < depth <= splits * chunk
+
+
 def test_missing_library_raises(monkeypatch, tmp_path):
     monkeypatch.setattr(wsw, "_lib", None)
     monkeypatch.setattr(wsw, "_LIB_PATH", str(tmp_path / "nope.so"))
