@@ -401,6 +401,18 @@ def _rates(torch, make, n, hot=True):
     return t, tp, th
 
 
+def _decode_attn_key(rows, peak):
+    """us per call and fraction of the HBM peak of the decode attention rows (per-head
+    layout, PDL-linked), for the key numbers; rows that are absent are left out."""
+    out = {}
+    for d in (32768, 65536):
+        for gq in (1, 8):
+            r = rows.get("attn_decode_d%d_g%d_per_head" % (d, gq))
+            if r:
+                out["d%d_g%d" % (d, gq)] = {"us": r["us_pdl"], "frac": round(r["GBps_pdl"] / peak, 4)}
+    return out
+
+
 def _entry(nbytes, t, tp, th=None, flops=None, **extra):
     """One bench row: us and GB/s (algorithmic bytes) per regime."""
     e = {"us": round(t * 1e6, 2), "GBps": round(nbytes / t / 1e9, 1),
@@ -964,6 +976,7 @@ def run_ours(args):
             key["windowed_q8_0_prefill_TFLOPs_pdl"] = {
                 "d32768_w4096": rows["windowed_q8_0_prefill_d32768_w4096"]["TFLOPs_pdl"],
                 "d65536_w8192": rows["windowed_q8_0_prefill_d65536_w8192"]["TFLOPs_pdl"]}
+            key["attn_decode_pdl"] = _decode_attn_key(rows, peak)
         if moe_steps is not None:
             key["config4_moe_step_us_pdl"] = {"T%d" % T: s["us_pdl"] for T, s in moe_steps.items()}
             key["config4_moe_step_GBps_pdl"] = {"T%d" % T: s["GBps_pdl"] for T, s in moe_steps.items()}
