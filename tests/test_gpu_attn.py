@@ -58,7 +58,7 @@ def _run_both_layouts(wsw, orc, q, k, v, scale, what, opts=None):
 
 
 @pytest.mark.parametrize("depth", [32768, 65536])
-@pytest.mark.parametrize("group", [1, 8])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])  # both forms: CUDA cores (1, 2), tensor cores (4, 8)
 def test_config_depths(orc, depth, group):
     wsw = need_gpu()
     q, k, v = _inputs(0, 4, group, depth)
