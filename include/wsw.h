@@ -327,8 +327,11 @@ int wsw_dequant_q8_0_kv(const int8_t *q, const uint16_t *d, int64_t depth, int64
  * K(h, p) is the row of head_dim binary16 values at k + h * k_head_stride +
  * p * k_pos_stride (elements); V likewise.  The per-head-contiguous scratch that
  * wsw_dequant_q8_0_kv writes has (pos, head) strides (head_dim, depth * head_dim), the
- * position-major cache (heads * head_dim, head_dim).  fp32 arithmetic; results agree
- * with fp64 within 1e-4 (normwise per output row), independent of the launch options.
+ * position-major cache (heads * head_dim, head_dim).  Groups of 1 and 2 compute in fp32;
+ * groups of 4 and 8 on the tensor cores, with q and the softmax weights entering as a
+ * binary16 high part plus a binary16 residual (about 22 bits) and fp32 accumulation.
+ * Either way results agree with fp64 within 1e-4 (normwise per output row) and do not
+ * depend on the launch options.
  *
  *   q      fp32 [heads][group][head_dim].
  *   k, v   binary16; 16-byte aligned, strides multiples of 8 elements.
